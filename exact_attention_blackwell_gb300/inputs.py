@@ -1,0 +1,99 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module holds no attention arithmetic: it only draws numbers.  Both sides of
+every parity check (the CUDA library and the CPU oracle) receive the same bf16
+tensors made here.
+
+Recipe (the pages print no dataset; every workload is synthetic):
+  * ``torch.Generator().manual_seed(seed)`` on the CPU; Q, K, V, dO drawn in that
+    order as iid N(0, 1) fp32, Q and dO with shape [B, N, H, d], K and V with
+    shape [B, N, Hkv, d].
+  * With ``outliers=True`` (the causal stress workload), after dO one uniform
+    draw per Q element then per K element; an element whose draw is < 0.01 is
+    multiplied by 20.
+  * Everything is then rounded to bf16 (round-to-nearest-even, torch default).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    outliers: bool = False
+    backward: bool = True
+    scale: float = field(default=float("nan"))
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d) if math.isnan(self.scale) else self.scale
+
+    def fwd_flops(self) -> float:
+        """4 B H N^2 d, halved when causal (the metric's convention)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops()
+
+
+def tiny() -> Workload:
+    return Workload("tiny B1 H2 N128 d64", 1, 2, 2, 128, 64, False, 0)
+
+
+def headline() -> Workload:
+    return Workload("B4 H16 N8192 d128 non-causal", 4, 16, 16, 8192, 128, False, 1)
+
+
+def causal_outliers() -> Workload:
+    return Workload("causal B8 H16 N4096 d128 1% x20 outliers", 8, 16, 16, 4096, 128, True, 2,
+                    outliers=True)
+
+
+def long_gqa() -> Workload:
+    return Workload("GQA B1 H32 Hkv8 N32768 d128 causal fwd", 1, 32, 8, 32768, 128, True, 3,
+                    backward=False)
+
+
+def sweep() -> list[Workload]:
+    out = []
+    k = 0
+    for d in (64, 128, 256):
+        for N in (1024, 4096, 16384):
+            for causal in (False, True):
+                B = 32768 // N
+                out.append(Workload(f"sweep d{d} N{N} B{B} {'causal' if causal else 'non-causal'}",
+                                    B, 16, 16, N, d, causal, 100 + k))
+                k += 1
+    return out
+
+
+def make_inputs(w: Workload, device="cpu", with_dO: bool = True):
+    """Returns dict(q, k, v, dO) of bf16 tensors on ``device`` (drawn on the CPU)."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.N, w.H, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.N, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.N, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    dO = torch.randn((w.B, w.N, w.H, w.d), generator=g, dtype=torch.float32) if with_dO or w.outliers else None
+    if w.outliers:
+        q = torch.where(torch.rand(q.shape, generator=g) < 0.01, q * 20.0, q)
+        k = torch.where(torch.rand(k.shape, generator=g) < 0.01, k * 20.0, k)
+    out = {"q": q, "k": k, "v": v, "dO": dO if with_dO else None}
+    return {n: (t.to(torch.bfloat16).to(device) if t is not None else None) for n, t in out.items()}
+
+
+def random_bf16(shape, seed: int, device="cpu"):
+    """iid N(0,1) rounded to bf16, for ad-hoc shapes (edge-case tests)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(device)

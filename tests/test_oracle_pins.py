@@ -1,0 +1,238 @@
+"""Pins for the CPU oracle: what the definition of attention fixes, checked
+without trusting the oracle itself (closed forms, invariants, brute force,
+finite differences, an independent numpy restatement, a worked example).
+
+CPU only; the shapes keep the whole file to a few seconds.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import np_ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def qkv(B, N, H, Hkv, d, seed):
+    return rnd((B, N, H, d), seed), rnd((B, N, Hkv, d), seed + 1), rnd((B, N, Hkv, d), seed + 2)
+
+
+# ---------------------------------------------------------------- worked example
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_two_token(oracle_mod, causal):
+    g = json.load(open(os.path.join(GOLDEN, "two_token.json")))
+    inp = g["inputs"]
+    env = {"e": math.e, "log": math.log}
+    ev = lambda a: np.array([[eval(x, env) for x in r] for r in a], dtype=np.float64)
+    q = np.array(inp["q"], float)[None, :, None, :]
+    k = np.array(inp["k"], float)[None, :, None, :]
+    v = np.array(inp["v"], float)[None, :, None, :]
+    dO = np.array(inp["dO"], float)[None, :, None, :]
+    exp = g["causal" if causal else "noncausal"]
+    o, lse = oracle_mod.attention_fwd(q, k, v, inp["scale"], causal)
+    np.testing.assert_allclose(o[0, :, 0, :], ev(exp["O"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], [eval(x, env) for x in exp["LSE"]], rtol=0, atol=1e-14)
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, dO, inp["scale"], causal)
+    np.testing.assert_allclose(dq[0, :, 0, :], ev(exp["dQ"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk[0, :, 0, :], ev(exp["dK"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv[0, :, 0, :], ev(exp["dV"]), rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_constant_o(oracle_mod, causal):
+    """Rows of P sum to 1: with every V row equal to u, every O row is u."""
+    q, k, _ = qkv(2, 33, 4, 2, 16, 10)
+    u = rnd((16,), 3)
+    v = np.broadcast_to(u, (2, 33, 2, 16)).copy()
+    o, _ = oracle_mod.attention_fwd(q, k, v, 0.3, causal)
+    np.testing.assert_allclose(o, np.broadcast_to(u, o.shape), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_q_gives_mean_of_visible_v(oracle_mod, causal):
+    B, N, H, d = 1, 17, 2, 8
+    _, k, v = qkv(B, N, H, H, d, 20)
+    q = np.zeros((B, N, H, d))
+    o, lse = oracle_mod.attention_fwd(q, k, v, 0.125, causal)
+    for i in range(N):
+        nvis = i + 1 if causal else N
+        np.testing.assert_allclose(o[0, i], v[0, :nvis].mean(axis=0), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, :, i], math.log(nvis), rtol=0, atol=1e-13)
+
+
+def test_causal_row0_is_v0(oracle_mod):
+    q, k, v = qkv(2, 9, 3, 3, 8, 30)
+    o, lse = oracle_mod.attention_fwd(q, k, v, 0.7, True)
+    np.testing.assert_allclose(o[:, 0], v[:, 0], rtol=0, atol=1e-14)
+    expect = 0.7 * np.einsum("bhc,bhc->bh", q[:, 0], k[:, 0])
+    np.testing.assert_allclose(lse[:, :, 0], expect, rtol=0, atol=1e-13)
+
+
+def test_single_key_gives_o_equals_v(oracle_mod):
+    q, k, v = qkv(3, 1, 2, 2, 8, 40)
+    o, lse = oracle_mod.attention_fwd(q, k, v, 0.5, False)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, 0.5 * np.einsum("bnhc,bnhc->bhn", q, k), rtol=0, atol=1e-13)
+
+
+def test_dominant_key_gives_one_hot(oracle_mod):
+    """A key aligned with q and scaled far beyond the rest makes P one-hot."""
+    B, N, H, d = 1, 12, 1, 4
+    q = np.zeros((B, N, H, d)); q[..., 0] = 1.0
+    k = rnd((B, N, H, d), 50) * 0.01
+    k[0, 5, 0, 0] = 2000.0
+    v = rnd((B, N, H, d), 51)
+    o, _ = oracle_mod.attention_fwd(q, k, v, 1.0, False)
+    np.testing.assert_allclose(o[0, :, 0], np.broadcast_to(v[0, 5, 0], (N, d)), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(oracle_mod, causal):
+    """Adding u to every key row leaves O unchanged and shifts LSE_i by scale q_i.u."""
+    B, N, H, d = 2, 21, 2, 8
+    q, k, v = qkv(B, N, H, H, d, 60)
+    u = rnd((d,), 61)
+    s = 0.4
+    o1, l1 = oracle_mod.attention_fwd(q, k, v, s, causal)
+    o2, l2 = oracle_mod.attention_fwd(q, k + u, v, s, causal)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, s * np.einsum("bnhc,c->bhn", q, u), rtol=0, atol=1e-12)
+    # dQ depends on keys only through differences k_j - k_j' (rows of dS sum to 0)
+    dO = rnd(q.shape, 62)
+    dq1, dk1, dv1 = oracle_mod.attention_bwd(q, k, v, dO, s, causal)
+    dq2, dk2, dv2 = oracle_mod.attention_bwd(q, k + u, v, dO, s, causal)
+    np.testing.assert_allclose(dq2, dq1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk2, dk1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv2, dv1, rtol=0, atol=1e-12)
+
+
+def test_kv_permutation_invariance(oracle_mod):
+    B, N, H, d = 1, 19, 2, 8
+    q, k, v = qkv(B, N, H, H, d, 70)
+    perm = np.random.default_rng(71).permutation(N)
+    o1, l1 = oracle_mod.attention_fwd(q, k, v, 0.3, False)
+    o2, l2 = oracle_mod.attention_fwd(q, k[:, perm], v[:, perm], 0.3, False)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+    dO = rnd(q.shape, 72)
+    dq1, dk1, dv1 = oracle_mod.attention_bwd(q, k, v, dO, 0.3, False)
+    dq2, dk2, dv2 = oracle_mod.attention_bwd(q, k[:, perm], v[:, perm], dO, 0.3, False)
+    np.testing.assert_allclose(dq2, dq1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk2, dk1[:, perm], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv2, dv1[:, perm], rtol=0, atol=1e-12)
+
+
+def test_causal_row_is_prefix_attention(oracle_mod):
+    """Brute force: causal row i equals non-causal attention over keys 0..i."""
+    B, N, H, d = 1, 13, 2, 8
+    q, k, v = qkv(B, N, H, H, d, 80)
+    o, lse = oracle_mod.attention_fwd(q, k, v, 0.5, True)
+    for i in range(N):
+        oi, li = oracle_mod.attention_fwd(q[:, : i + 1], k[:, : i + 1], v[:, : i + 1], 0.5, False)
+        np.testing.assert_allclose(o[:, i], oi[:, i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], li[:, :, i], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_repeated_kv(oracle_mod, causal):
+    """Query head h reads kv head h // (H/Hkv); the gradient of a shared kv head
+    is the sum over its query heads."""
+    B, N, H, Hkv, d = 2, 11, 6, 2, 8
+    q, k, v = qkv(B, N, H, Hkv, d, 90)
+    dO = rnd(q.shape, 91)
+    kr, vr = np.repeat(k, 3, axis=2), np.repeat(v, 3, axis=2)
+    o1, l1 = oracle_mod.attention_fwd(q, k, v, 0.3, causal)
+    o2, l2 = oracle_mod.attention_fwd(q, kr, vr, 0.3, causal)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+    dq1, dk1, dv1 = oracle_mod.attention_bwd(q, k, v, dO, 0.3, causal)
+    dq2, dk2, dv2 = oracle_mod.attention_bwd(q, kr, vr, dO, 0.3, causal)
+    np.testing.assert_allclose(dq1, dq2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk1, dk2.reshape(B, N, Hkv, 3, d).sum(3), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv1, dv2.reshape(B, N, Hkv, 3, d).sum(3), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_linearity_in_v(oracle_mod, causal):
+    """O is linear in V: dV does not change with V -> cV, dQ and dK scale by c;
+    and the key gradients of one head sum to zero over the keys."""
+    q, k, v = qkv(1, 15, 2, 2, 8, 100)
+    dO = rnd(q.shape, 101)
+    dq1, dk1, dv1 = oracle_mod.attention_bwd(q, k, v, dO, 0.35, causal)
+    dq2, dk2, dv2 = oracle_mod.attention_bwd(q, k, 2.5 * v, dO, 0.35, causal)
+    np.testing.assert_allclose(dv2, dv1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dq2, 2.5 * dq1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk2, 2.5 * dk1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk1.sum(axis=1), 0.0, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- finite differences
+@pytest.mark.parametrize("H,Hkv,causal", [(1, 1, False), (2, 2, True), (2, 1, False), (2, 1, True)])
+def test_backward_matches_finite_differences(oracle_mod, H, Hkv, causal):
+    B, N, d = 1, 6, 5
+    q, k, v = qkv(B, N, H, Hkv, d, 110 + H + 3 * Hkv + causal)
+    dO = rnd(q.shape, 120)
+    s = 0.6
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, dO, s, causal)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle_mod.attention_fwd(q_, k_, v_, s, causal)
+        return float((o * dO).sum())
+
+    h = 1e-5
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{f"{a}_": b for a, b in args_p.items()})
+                        - loss(**{f"{a}_": b for a, b in args_m.items()})) / (2 * h)
+        err = np.abs(num - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+# ---------------------------------------------------------------- independent restatement
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", [(1, 128, 2, 2, 64, False), (2, 37, 4, 2, 16, True),
+                                                (1, 50, 3, 1, 32, False), (1, 64, 2, 2, 8, True)])
+def test_c_oracle_matches_numpy_restatement(oracle_mod, B, N, H, Hkv, d, causal):
+    q, k, v = qkv(B, N, H, Hkv, d, 130 + N)
+    dO = rnd(q.shape, 131)
+    s = 1.0 / math.sqrt(d)
+    o1, l1 = oracle_mod.attention_fwd(q, k, v, s, causal)
+    o2, l2 = np_ref.fwd(q, k, v, s, causal)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+    g1 = oracle_mod.attention_bwd(q, k, v, dO, s, causal)
+    g2 = np_ref.bwd(q, k, v, dO, s, causal)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_selection_matches_full(oracle_mod, causal):
+    B, N, H, Hkv, d = 2, 40, 4, 2, 8
+    q, k, v = qkv(B, N, H, Hkv, d, 140)
+    dO = rnd(q.shape, 141)
+    rows = np.array([39, 0, 17, 5])
+    o, l = oracle_mod.attention_fwd(q, k, v, 0.3, causal)
+    os_, ls_ = oracle_mod.attention_fwd(q, k, v, 0.3, causal, rows=rows)
+    np.testing.assert_array_equal(os_, o[:, rows])
+    np.testing.assert_array_equal(ls_, l[:, :, rows])
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, dO, 0.3, causal)
+    dqs, dks, dvs = oracle_mod.attention_bwd(q, k, v, dO, 0.3, causal, qrows=rows, kvrows=rows[::-1])
+    np.testing.assert_array_equal(dqs, dq[:, rows])
+    np.testing.assert_array_equal(dks, dk[:, rows[::-1]])
+    np.testing.assert_array_equal(dvs, dv[:, rows[::-1]])
