@@ -1,0 +1,144 @@
+"""Fused exact attention for NVIDIA GB300 (sm_103a): Python binding.
+
+The compute lives in ``libfa_gb300.so`` (hand-written CUDA, C ABI declared in
+``include/fa.h``).  This module only marshals arguments: every function with a
+C name calls the C entry point of the same name and returns its status code;
+the ``attention_*`` helpers allocate outputs with torch and raise
+:class:`FaError` on a non-zero status.  There is no fallback: if the library is
+missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ALIGNMENT = -3
+FA_ERR_WORKSPACE = -4
+FA_ERR_CUDA = -5
+FA_ERR_TIMEOUT = -6
+
+# name -> (restype, argtypes) for every symbol include/fa.h declares
+_P, _I, _F, _LL, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_exp2_poly": (_I, [_P, _P, _LL, _P]),
+    "fa_last_device_status": (_I, [_P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with exact_attention_blackwell_gb300.build.build()")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------------ C names
+def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
+    return lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, float(scale),
+                        int(bool(causal)), _stream(stream))
+
+
+def fa_bwd_workspace_bytes(B, H, Hkv, N, d) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, Hkv, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes,
+           stream=None) -> int:
+    return lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B,
+                        H, Hkv, N, d, float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
+                        _stream(stream))
+
+
+def fa_exp2_poly(x, y, n, stream=None) -> int:
+    return lib().fa_exp2_poly(_ptr(x), _ptr(y), int(n), _stream(stream))
+
+
+def fa_last_device_status(stream=None) -> int:
+    return lib().fa_last_device_status(_stream(stream))
+
+
+# ------------------------------------------------------------------ torch helpers
+def _dims(q, k):
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    return B, N, H, Hkv, d
+
+
+def attention_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """q [B,N,H,d], k/v [B,N,Hkv,d] bf16 CUDA tensors -> (o bf16, lse fp32 [B,H,N])."""
+    import torch
+
+    B, N, H, Hkv, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def attention_bwd(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None):
+    """Returns (dq, dk, dv) bf16."""
+    import torch
+
+    B, N, H, Hkv, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa_bwd_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace.numel(),
+                stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv

@@ -1,0 +1,223 @@
+// fa_api.cu — the C ABI (include/fa.h): argument checks, tensor-map encoding,
+// launches, the device status word and the standalone software-exp2 kernel.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "exp2_poly.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+
+// [0] error bits (1 = a bounded wait ran out), [1] id of the first wait site
+// that ran out, [2] number of warp-level O rescales (forward), [3] spare.
+static __device__ unsigned g_status[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices] = {};
+int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 GB300, -1 other
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device(int *dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+// Once per device: compute capability must be 10.3 (GB300, sm_103a).
+int check_device() {
+  int dev;
+  if (current_device(&dev) != FA_OK) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_dev_ok[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int Hkv, int N, int d, float scale) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  // element offsets of [B, N, H, d] must fit the 2^31 range used for row indices
+  if ((long long)B * N * H * d >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+unsigned *device_status_ptr() {
+  int dev;
+  if (current_device(&dev) != FA_OK) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned *>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hx, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hx * d * 2, (cuuint64_t)N * Hx * d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+namespace {
+
+__global__ void exp2_poly_kernel(const float *__restrict__ x, float *__restrict__ y, long long n) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) y[i] = exp2_poly(x[i]);
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void *stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FA_ERR_ALIGNMENT;
+  if ((rc = check_device()) != FA_OK) return rc;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (encode_bf16_tile_map(&p.tm_q, q, B, N, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
+      encode_bf16_tile_map(&p.tm_v, v, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_o, o, B, N, H, d, 128))
+    return FA_ERR_CUDA;
+  p.lse = lse;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_fwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {
+  if (check_common(B, H, Hkv, N, d, 1.0f) != FA_OK) return 0;
+  const size_t acc = (size_t)B * N * H * d * sizeof(float);
+  const size_t rows = (size_t)B * H * N * sizeof(float);
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return up(acc) + 2 * up(rows);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
+           void *dk, void *dv, int B, int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
+           size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_ALIGNMENT;
+  const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_WORKSPACE;
+  if ((rc = check_device()) != FA_OK) return rc;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (encode_bf16_tile_map(&p.tm_q, q, B, N, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
+      encode_bf16_tile_map(&p.tm_v, v, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_do, dO, B, N, H, d, 128) ||
+      encode_bf16_tile_map(&p.tm_dk, dk, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_dv, dv, B, N, Hkv, d, 128))
+    return FA_ERR_CUDA;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *dq_acc = reinterpret_cast<float *>(ws);
+  float *lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
+  float *delta = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(lse2) + up((size_t)B * H * N * sizeof(float)));
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_bwd(p, d, causal != 0, o, dO, lse, dq, lse2, delta, static_cast<cudaStream_t>(stream));
+}
+
+int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u)) return FA_ERR_ALIGNMENT;
+  if (n == 0) return FA_OK;
+  int rc = check_device();
+  if (rc != FA_OK) return rc;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
+  const long long want = (n + 255) / 256;
+  const int blocks = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);
+  exp2_poly_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_last_device_status(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned *st = device_status_ptr();
+  if (!st) return FA_ERR_CUDA;
+  unsigned h[2] = {0, 0};
+  if (cudaMemcpy(h, st, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (h[0] != 0) {
+    const unsigned zero[2] = {0, 0};
+    if (cudaMemcpy(st, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,403 @@
+// fa_fwd.cu — fused attention forward for sm_103a.
+//
+// One CTA owns QT query tiles of 128 rows of one (batch, head) and streams the
+// key/value blocks of 128 rows past them:
+//   S_t = Q_t K_j^T      tcgen05 MMA, accumulated in TMEM          (FA4 paper
+//   P_t = 2^(S_t - m)    softmax warps, online row max / row sum    summary,
+//   O_t += P_t V_j       tcgen05 MMA, P read from TMEM             section 2.A)
+// so the N x N scores never leave the SM (FlashAttention-3 page, "FlashAttention
+// y FlashAttention-2": tiling plus fusion).
+//
+// Warp roles (FA4 paper summary, section 2.A: producers, softmax consumers,
+// specialised warps; FlashAttention-3 page, section 1: producer/consumer warps):
+//   warps 0..4*QT-1 : softmax, one warpgroup per query tile, one thread per row;
+//                     also the conditional O rescale and the epilogue
+//   warp  4*QT      : MMA issue (one thread) and TMEM allocation
+//   warp  4*QT+1    : TMA producer (one thread): Q once, then K_j, V_j into a
+//                     STAGES-deep shared-memory ring
+//
+// MMA order per key block j (two query tiles):  PV_0,j  S_0,j+1  PV_1,j  S_1,j+1
+// so that each softmax warpgroup works while the tensor core runs the other
+// tile's two MMAs (the ping-pong idea of the FlashAttention-3 page, section 1,
+// carried over to asynchronous tcgen05 MMAs).  P_t is written over the first 64
+// columns of S_t in TMEM; the tensor pipe executes one thread's MMAs in order, so
+// S_t,j+1 never overwrites P_t,j before PV_t,j has read it.
+//
+// Softmax (FA4 paper summary, section 2.B): 2^x on MUFU.EX2 for most columns and
+// on the FMA pipe (exp2_poly) for FA_FWD_POLY_PER16 of every 16; the running
+// maximum m_ref is only moved (with an O rescale) when a new block's maximum
+// exceeds it by more than kRescaleTau.  The result is exact either way: O and l
+// share the same stale m_ref, and O / l and m_ref + log2 l are what is stored.
+#include "exp2_poly.cuh"
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kQT = (D <= 128) ? 2 : 1;  // query tiles per CTA
+  static constexpr int kStages = (D == 64) ? 6 : (D == 128 ? 4 : 2);
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile of Q, K, V or O
+  static constexpr int kBoxes = D / 64;           // 64-column TMA boxes per tile (16 KB each)
+  static constexpr int kThreads = 128 * kQT + 64;
+  static constexpr int kMmaWarp = 4 * kQT;
+  static constexpr int kLoadWarp = 4 * kQT + 1;
+  static constexpr int kOCol = 128 * kQT;  // TMEM column of O_0 (S_t at 128 t)
+  static constexpr int kTmemCols = 512;
+  static_assert(kOCol + kQT * D <= kTmemCols, "TMEM budget");
+  // shared memory (offsets from a 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = kQT * kTileBytes;
+  static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
+  // barriers: full[S], empty[S], q_full, s_full[QT], p_full[QT], o_full[QT], drain
+  static constexpr int kNumBars = 2 * kStages + 2 + 3 * kQT;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+enum WaitSite : int {
+  kSiteQ = 1, kSiteKFull = 2, kSiteVFull = 3, kSitePFull = 4, kSiteEmpty = 5,
+  kSiteSFull = 6, kSiteOFull = 7, kSiteDrain = 8
+};
+
+template <int D, bool CAUSAL, int POLY16>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int QT = C::kQT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  const uint32_t q_bar = bar0 + 8u * (2 * C::kStages);
+  auto s_bar = [&](int t) { return bar0 + 8u * (2 * C::kStages + 1 + t); };
+  auto p_bar = [&](int t) { return bar0 + 8u * (2 * C::kStages + 1 + QT + t); };
+  auto o_bar = [&](int t) { return bar0 + 8u * (2 * C::kStages + 1 + 2 * QT + t); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 1 + 3 * QT);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // heaviest first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / (p.H / p.Hkv);
+  const int n_kv_all = (p.N + 127) / 128;
+
+  int q0[QT], nb[QT];
+  int nb_max = 0;
+#pragma unroll
+  for (int t = 0; t < QT; ++t) {
+    q0[t] = (group * QT + t) * 128;
+    if (q0[t] >= p.N) nb[t] = 0;
+    else nb[t] = CAUSAL ? (min(q0[t] + 127, p.N - 1) / 128 + 1) : n_kv_all;
+    nb_max = max(nb_max, nb[t]);
+  }
+
+  if (threadIdx.x == 0) {
+    // p_full[t] collects one arrival per softmax thread; every other barrier one.
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const uint32_t bar = bar0 + 8u * i;
+      const bool is_p = bar >= p_bar(0) && bar < p_bar(0) + 8u * QT;
+      mbar_init(bar, is_p ? 128u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4 * QT) {
+    // ===================================================== softmax warpgroups
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + 128u * t;
+    const uint32_t o_tm = tmem + lane_off + C::kOCol + (uint32_t)(D * t);
+    const int q_row = q0[t] + r;
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY;  // running maximum, scaled log2 units
+    float l_sum = 0.f;        // running row sum relative to m_ref
+    bool ok = true;
+    unsigned rescales = 0;
+
+    for (int j = 0; j < nb[t] && ok; ++j) {
+      ok = mbar_wait_warp(s_bar(t), j & 1, wctx, kSiteSFull);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(s_tm + 32 * c, sr[c]);
+      tmem_wait_ld(sr[0]);
+      reg_tie(sr[1]);
+      reg_tie(sr[2]);
+      reg_tie(sr[3]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int kv0 = j * 128;
+      const bool need_mask = (kv0 + 128 > p.N) || (CAUSAL && kv0 + 127 > q0[t]);
+      if (need_mask) {
+        const int lim = CAUSAL ? min(p.N - 1, q_row) - kv0 : p.N - 1 - kv0;  // last visible column
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+      if (j == 0) {
+        m_ref = m_blk;
+      } else {
+        const bool need = (m_blk - m_ref) > kRescaleTau;
+        if (__any_sync(0xffffffffu, need)) {
+          // Whole warp rescales (tcgen05.ld/st are warp-collective); rows whose
+          // maximum did not move use alpha = 1.  PV_t,j-1 is complete: its
+          // commit preceded S_t,j's.
+          const float m_new = fmaxf(m_ref, m_blk);
+          const float alpha = ex2_mufu(m_ref - m_new);
+          m_ref = m_new;
+          l_sum *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(o_tm + 16 * c, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_32x32b_x16(o_tm + 16 * c, o);
+          }
+          rescales += (lane == 0);
+        }
+      }
+      const float neg_m = -m_ref;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float x = fmaf(s[64 * half + c + u], c2, neg_m);
+            e[u] = ((c + u) % 16 < POLY16) ? exp2_poly(x) : ex2_mufu(x);
+          }
+          l0 += e[0];
+          l1 += e[1];
+          l2 += e[2];
+          l3 += e[3];
+          pk[c >> 1] = pack_bf16x2(e[0], e[1]);
+          pk[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
+        }
+        tmem_st_32x32b_x32(s_tm + 32 * half, pk);
+      }
+      l_sum += (l0 + l1) + (l2 + l3);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_bar(t));
+    }
+
+    // ----------------------------------------------------- epilogue
+    if (nb[t] > 0) {
+      if (ok) ok = mbar_wait_warp(o_bar(t), 0, wctx, kSiteOFull);
+      tc_fence_after();
+      uint8_t *stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is dead once O_t is final
+      if (ok) {
+        const float inv_l = 1.0f / l_sum;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(o_tm + 32 * c, o);
+          tmem_wait_ld(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          const int box = c >> 1;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int chunk = ((c & 1) * 4 + k4) ^ (r & 7);
+            uint4 *dst = reinterpret_cast<uint4 *>(stage + box * 16384 + r * 128 + chunk * 16);
+            *dst = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+          }
+        }
+        if (p.lse != nullptr && q_row < p.N)
+          p.lse[((size_t)b * p.H + h) * p.N + q_row] = (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+      }
+      fence_proxy_async_smem();
+      if (t == 0) named_bar_sync(1, 128);
+      else named_bar_sync(2, 128);
+      if (r == 0 && ok) {
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, q0[t], b);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+    }
+    if (rescales) atomicAdd(p.status + 2, rescales);
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, D, false, true);
+      const uint32_t q_smem = sbase + C::kOffQ;
+      const uint32_t ring = sbase + C::kOffRing;
+      auto slot_of = [&](int fill) { return fill % C::kStages; };
+      auto par_of = [&](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
+      auto issue_s = [&](int t, uint32_t k_smem) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + 128u * t, make_sdesc_sw128(q_smem + t * C::kTileBytes + off, 0, 1024),
+                 make_sdesc_sw128(k_smem + off, 0, 1024), idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t v_smem, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kOCol + (uint32_t)(D * t), tmem + 128u * t + 8u * kk,
+                 make_sdesc_sw128(v_smem + kk * 2048, 16384, 1024), idesc_pv, (acc || kk > 0));
+      };
+      bool ok = nb_max > 0;
+      if (ok) ok = mbar_wait(q_bar, 0, wctx, kSiteQ);
+      if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), wctx, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < QT; ++t)
+          if (nb[t] > 0) {
+            issue_s(t, ring + slot_of(0) * C::kTileBytes);
+            tc_commit(s_bar(t));
+          }
+        tc_commit(empty_bar(slot_of(0)));
+      }
+      for (int j = 0; j < nb_max && ok; ++j) {
+        const int fv = 2 * j + 1, fk = 2 * j + 2;
+        ok = mbar_wait(full_bar(slot_of(fv)), par_of(fv), wctx, kSiteVFull);
+        if (!ok) break;
+        tc_fence_after();
+        bool k_next = false;
+        for (int t = 0; t < QT && ok; ++t) {
+          if (j >= nb[t]) continue;
+          ok = mbar_wait(p_bar(t), j & 1, wctx, kSitePFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, ring + slot_of(fv) * C::kTileBytes, j > 0);
+          if (j + 1 < nb[t]) {
+            if (!k_next) {
+              ok = mbar_wait(full_bar(slot_of(fk)), par_of(fk), wctx, kSiteKFull);
+              if (!ok) break;
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, ring + slot_of(fk) * C::kTileBytes);
+            tc_commit(s_bar(t));
+          } else {
+            tc_commit(o_bar(t));
+          }
+        }
+        tc_commit(empty_bar(slot_of(fv)));
+        if (k_next) tc_commit(empty_bar(slot_of(fk)));
+      }
+      // Drain: every MMA this thread issued completes before TMEM is released.
+      tc_commit(drain_bar);
+      WaitCtx drain_ctx{abort_flag, p.status};
+      if (!mbar_wait(drain_bar, 0, drain_ctx, kSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();  // aborted: still give in-flight MMAs time to land
+        while (!mbar_test(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer
+    if (lane == 0 && nb_max > 0) {
+      const uint32_t q_smem = sbase + C::kOffQ;
+      const uint32_t ring = sbase + C::kOffRing;
+      const uint64_t keep = policy_evict_last();   // K/V are re-read by the other query tiles
+      const uint64_t once = policy_evict_first();  // Q is read once
+      int nq = 0;
+      for (int t = 0; t < QT; ++t) nq += (nb[t] > 0);
+      mbar_arrive_expect_tx(q_bar, nq * C::kTileBytes);
+      for (int t = 0; t < QT; ++t)
+        if (nb[t] > 0)
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d_hint(q_smem + t * C::kTileBytes + bx * 16384, &p.tm_q, q_bar, bx * 64, h, q0[t], b, once);
+      bool ok = true;
+      int fill = 0;
+      for (int j = 0; j < nb_max && ok; ++j) {
+        for (int kv = 0; kv < 2 && ok; ++kv, ++fill) {
+          const int s = fill % C::kStages;
+          ok = mbar_wait(empty_bar(s), ((fill / C::kStages) & 1) ^ 1, wctx, kSiteEmpty);
+          if (!ok) break;
+          mbar_arrive_expect_tx(full_bar(s), C::kTileBytes);
+          const CUtensorMap *map = kv ? &p.tm_v : &p.tm_k;
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d_hint(ring + s * C::kTileBytes + bx * 16384, map, full_bar(s), bx * 64, kh, j * 128, b, keep);
+        }
+      }
+      // Every copy issued lands before the CTA exits (normally they already have).
+      const uint64_t t0 = global_timer_ns();
+      for (int f = max(0, fill - C::kStages); f < fill; ++f)
+        while (!mbar_test(full_bar(f % C::kStages), (f / C::kStages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16>;
+  static bool configured = false;  // per process; attribute is per function
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FA_ERR_CUDA;
+    configured = true;
+  }
+  const int rows_per_cta = 128 * C::kQT;
+  dim3 grid((p.N + rows_per_cta - 1) / rows_per_cta, p.H, p.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream) {
+  switch (d) {
+    case 64: return causal ? launch_fwd_t<64, true>(p, stream) : launch_fwd_t<64, false>(p, stream);
+    case 128: return causal ? launch_fwd_t<128, true>(p, stream) : launch_fwd_t<128, false>(p, stream);
+    case 256: return causal ? launch_fwd_t<256, true>(p, stream) : launch_fwd_t<256, false>(p, stream);
+    default: return FA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,60 @@
+// fa_internal.h — declarations shared by the translation units of the library
+// (not part of the public C ABI in include/fa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Software-exp2 share: of every 16 score columns, this many are exponentiated
+// with the FMA-pipe polynomial and the rest with MUFU.EX2.
+#ifndef FA_FWD_POLY_PER16
+#define FA_FWD_POLY_PER16 0
+#endif
+
+// Conditional-rescale threshold tau, log2 units (FlashAttention-4 paper
+// summary, section 2.B: rescale only when the running maximum moves by more
+// than a threshold; the pages give no value).
+constexpr float kRescaleTau = 8.0f;
+
+struct FwdParams {
+  CUtensorMap tm_q;  // [B, N, H, d] bf16, box 128 rows x 64 cols, 128B swizzle
+  CUtensorMap tm_k;  // [B, N, Hkv, d]
+  CUtensorMap tm_v;  // [B, N, Hkv, d]
+  CUtensorMap tm_o;  // [B, N, H, d] (store)
+  float *lse;        // [B, H, N] or nullptr
+  unsigned *status;  // device status word: [0] error bits, [1] failing site, [2] rescale count
+  int B, H, Hkv, N;
+  float scale_log2;  // scale * log2(e)
+};
+
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
+  CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
+  const float *lse2;                    // [B, H, N] LSE * log2(e)
+  const float *delta;                   // [B, H, N] D = rowsum(dO * O)
+  float *dq_acc;                        // [B, N, H, d] fp32 accumulator
+  unsigned *status;
+  int B, H, Hkv, N;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+};
+
+// Device status word of the current device (a small static device array).
+unsigned *device_status_ptr();
+
+// Encodes a 4-D tensor map over a bf16 [B, N, Hx, d] tensor, box = 64 columns x
+// `box_rows` rows of one head, 128-byte swizzle.  Returns 0 on success.
+int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows);
+
+int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream);
+int launch_bwd(const BwdParams &p, int d, bool causal, const void *o, const void *dO, const float *lse,
+               void *dq, float *lse2_ws, float *delta_ws, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,103 @@
+/*
+ * fa.h — C ABI of the fused exact-attention library for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (FlashAttention-4 article, "Por que el enfoque estandar ya
+ * no funciona": the two products S = Q K^T and O = P V with a softmax between
+ * them; FlashAttention-3 page, "FlashAttention y FlashAttention-2": tiled and
+ * fused so the N x N score matrix never reaches global memory).  For every
+ * batch b, query head h, query row i, with kh = h / (H / Hkv):
+ *
+ *     s_ij  = scale * q_i . k_j                 (j visible iff !causal || j <= i)
+ *     O_i   = sum_j softmax_j(s_i.) v_j,        LSE_i = ln sum_{visible j} exp(s_ij)
+ *
+ * and the backward pass of L = sum(dO * O):
+ *
+ *     dV_j = sum_i P_ij dO_i,  dP_ij = dO_i . v_j,  D_i = dO_i . O_i,
+ *     dS_ij = P_ij (dP_ij - D_i),  dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i
+ *
+ * (the pages list the backward's bottlenecks, FlashAttention-4 paper summary,
+ * section 2.C, but not its formulas; these follow from the forward by the chain
+ * rule).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory for them and keeps no reference after return.
+ *   - Layouts are dense, row-major, no strides:
+ *         q, o, dq, dO : bf16 [B, N, H,   d]
+ *         k, v, dk, dv : bf16 [B, N, Hkv, d]
+ *         lse          : fp32 [B, H, N]      (natural-log units)
+ *   - Every tensor base pointer must be 16-byte aligned (tensor-memory-access
+ *     copies require it).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *     asynchronous: it validates, enqueues and returns.
+ *   - Supported: d in {64, 128, 256}; N >= 1 (any length, ragged tails are
+ *     masked); B, H, Hkv >= 1 with H % Hkv == 0; scale finite and > 0; B*H and
+ *     B*Hkv below 65536.  Device: compute capability 10.3 (GB300).
+ *   - Outputs must not alias inputs (not checked).
+ *   - Errors: every argument check happens before any launch and nothing is
+ *     written on error.  A launch failure returns FA_ERR_CUDA.  Faults inside a
+ *     kernel surface asynchronously at the caller's next synchronisation.  Every
+ *     wait inside the kernels is bounded: a wait that runs out sets a status
+ *     word that fa_last_device_status() reports, and the kernel returns.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad scale, H % Hkv != 0 */
+  FA_ERR_UNSUPPORTED = -2, /* head dim not in {64,128,256}, sizes beyond limits, not a GB300 */
+  FA_ERR_ALIGNMENT = -3,   /* a tensor pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than fa_bwd_workspace_bytes() */
+  FA_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+  FA_ERR_TIMEOUT = -6      /* a bounded wait inside a kernel ran out (reported by fa_last_device_status) */
+} fa_status;
+
+/* Forward pass.  Writes o [B,N,H,d] bf16 and lse [B,H,N] fp32 (natural log).
+ * `lse` may be NULL when the caller does not need it (no backward). */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
+
+/* Bytes of device workspace fa_bwd needs for these sizes (fp32 dQ accumulator
+ * [B,N,H,d] plus fp32 row terms [B,H,N] for D and the log2-scaled LSE).
+ * Returns 0 for sizes fa_bwd would reject. */
+size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d);
+
+/* Backward pass.  Inputs q, k, v, o, lse from the forward, and dO [B,N,H,d].
+ * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  `workspace` is caller
+ * owned device memory of at least fa_bwd_workspace_bytes() bytes, 256-byte
+ * aligned; its contents on entry do not matter and are overwritten.  The call
+ * is not deterministic in the last bits (dQ is summed with atomics). */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dO, void *dq, void *dk, void *dv,
+           int B, int H, int Hkv, int N, int d, float scale, int causal,
+           void *workspace, size_t workspace_bytes, void *stream);
+
+/* The software 2^x the forward kernel evaluates on the FMA pipe (FlashAttention-4
+ * paper summary, section 2.B: 2^x emulated with FMA instructions, a polynomial
+ * of degree 3 to 5 for the fractional part).  Range reduction x = j + f with
+ * j = rint(x), |f| <= 1/2; a degree-3 minimax polynomial for 2^f; 2^j inserted
+ * into the exponent.  Evaluates y[i] = 2^x[i] for n fp32 values on `stream`
+ * (device pointers, 4-byte aligned).  Valid for x <= 64; x below -150 or -inf
+ * gives +0.  Exposed so that its accuracy can be checked exhaustively. */
+int fa_exp2_poly(const float *x, float *y, long long n, void *stream);
+
+/* Synchronises `stream`, then returns FA_OK or FA_ERR_TIMEOUT if a bounded wait
+ * in any kernel of this library on the current device ran out since the last
+ * call (and clears the flag).  Returns FA_ERR_CUDA if synchronisation fails. */
+int fa_last_device_status(void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

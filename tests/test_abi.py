@@ -1,0 +1,105 @@
+"""The C ABI, without a GPU: the library loads, exports every entry point that
+include/fa.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_blackwell_gb300 as fa
+from exact_attention_blackwell_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_exp2_poly", "fa_last_device_status",
+              "fa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in fa.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "FA_OK"), (-1, "FA_ERR_INVALID_ARG"), (-2, "FA_ERR_UNSUPPORTED"),
+                       (-3, "FA_ERR_ALIGNMENT"), (-4, "FA_ERR_WORKSPACE"), (-5, "FA_ERR_CUDA"),
+                       (-6, "FA_ERR_TIMEOUT"), (7, "FA_ERR_UNKNOWN")]:
+        assert fa.status_string(code) == name
+
+
+A = 0x10000  # a 16-byte aligned fake device address: never dereferenced, calls fail validation first
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(H=6, Hkv=4), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_ALIGNMENT),
+    (dict(o=A + 2), fa.FA_ERR_ALIGNMENT),
+    (dict(lse=A + 2), fa.FA_ERR_ALIGNMENT),
+])
+def test_fwd_rejects_bad_arguments(lib, args, code):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Hkv=2, N=128, d=128, scale=0.125, causal=0)
+    a.update(args)
+    assert fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["N"], a["d"],
+                     a["scale"], a["causal"], 0) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(dq=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(H=3, Hkv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(dk=A + 4), fa.FA_ERR_ALIGNMENT),
+    (dict(ws=None), fa.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=100), fa.FA_ERR_WORKSPACE),
+    (dict(ws=A + 16), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_rejects_bad_arguments(lib, args, code):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=2, Hkv=2, N=256, d=128, scale=0.1,
+             causal=1, ws=A, ws_bytes=None)
+    a.update(args)
+    nbytes = fa.fa_bwd_workspace_bytes(a["B"], a["H"], a["Hkv"], a["N"], 128)
+    wsb = nbytes if a["ws_bytes"] is None else a["ws_bytes"]
+    assert fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dO"], a["dq"], a["dk"], a["dv"], a["B"],
+                     a["H"], a["Hkv"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], wsb, 0) == code
+
+
+def test_workspace_size():
+    B, H, Hkv, N, d = 2, 4, 2, 1000, 128
+    up = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d) == up(B * N * H * d * 4) + 2 * up(B * H * N * 4)
+    assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, 96) == 0
+    assert fa.fa_bwd_workspace_bytes(0, H, Hkv, N, d) == 0
+
+
+def test_exp2_rejects_bad_arguments(lib):
+    assert fa.fa_exp2_poly(None, None, 5, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_exp2_poly(A, A, -1, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_exp2_poly(A + 1, A, 5, 0) == fa.FA_ERR_ALIGNMENT
+    assert fa.fa_exp2_poly(None, None, 0, 0) == fa.FA_OK
