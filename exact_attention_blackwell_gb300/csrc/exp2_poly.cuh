@@ -24,7 +24,8 @@ __device__ __forceinline__ float mul_rn_noftz(float a, float b) {
   return r;
 }
 
-// 2^x for x <= 64; x < -150 (including -inf) returns +0.
+// 2^x for x <= 63 (2^(j+64) must stay below the fp32 exponent limit);
+// x < -150 (including -inf) returns +0.
 __device__ __forceinline__ float exp2_poly(float x) {
   constexpr float kShift = 12582912.0f + 64.0f;  // 1.5 * 2^23 + 64
   x = fmaxf(x, -150.0f);

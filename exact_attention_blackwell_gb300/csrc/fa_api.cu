@@ -134,8 +134,9 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {
   if (check_common(B, H, Hkv, N, d, 1.0f) != FA_OK) return 0;
+  const size_t Npad = ((size_t)N + 127) / 128 * 128;
   const size_t acc = (size_t)B * N * H * d * sizeof(float);
-  const size_t rows = (size_t)B * H * N * sizeof(float);
+  const size_t rows = (size_t)B * H * Npad * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   return up(acc) + 2 * up(rows);
 }
@@ -163,7 +164,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *dq_acc = reinterpret_cast<float *>(ws);
   float *lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
-  float *delta = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(lse2) + up((size_t)B * H * N * sizeof(float)));
+  const size_t Npad = ((size_t)N + 127) / 128 * 128;
+  float *delta = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(lse2) + up((size_t)B * H * Npad * sizeof(float)));
   p.lse2 = lse2;
   p.delta = delta;
   p.dq_acc = dq_acc;

@@ -68,7 +68,7 @@ struct WaitCtx {
   unsigned *status;     // device status word: [0] = error bits, [1] = first failing site
 };
 
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     for (int i = 0; i < 128; ++i)

