@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention hot path: one step = forward + backward of
+the workload (default: B=4, H=16, N=8192, d=128, non-causal, bf16), inputs
+resident in HBM, timed with CUDA events.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload headline|causal|gqa]
+
+--impl reference times the fp64 CPU oracle (a deliberately slow, plain
+statement of the same computation) on the host cores: each step is the forward
+and backward of one (batch, head) slice of the same workload.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+copy of the workload (attention heads shard with no exchange), so scaling is
+weak and `value` is the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPs/s fwd & bwd (bf16, d=128) at 1 GB300; fraction of 2.25 PF BF16 peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def workload(name: str):
+    from exact_attention_blackwell_gb300 import inputs
+
+    return {"headline": inputs.headline, "causal": inputs.causal_outliers, "gqa": inputs.long_gqa}[name]()
+
+
+def env_int(k, default):
+    try:
+        return int(os.environ.get(k, default))
+    except ValueError:
+        return default
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+                power.append(float(row[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ peaks and profiles
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"sustained": float(j["bf16_tflops_sustained"]), "burst": float(j["bf16_tflops"]),
+                "hbm_gbs": float(j["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+    except (OSError, KeyError, ValueError):
+        return {"sustained": 1700.0, "burst": 1900.0, "hbm_gbs": 6800.0, "source": "fallback (no measured file)"}
+
+
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "exact_attention_blackwell_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != src_hash:
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def cpu_oracle_step(x, w, head: int):
+    """fwd + bwd of one (b, h) slice with the fp64 oracle; returns seconds."""
+    import oracle
+
+    b, h = divmod(head % (w.B * w.H), w.H)
+    kh = h // (w.H // w.Hkv)
+    q = x["q"][b:b + 1, :, h:h + 1]
+    k = x["k"][b:b + 1, :, kh:kh + 1]
+    v = x["v"][b:b + 1, :, kh:kh + 1]
+    dO = x["dO"][b:b + 1, :, h:h + 1] if x["dO"] is not None else None
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, w.sm_scale, w.causal)
+    if w.backward:
+        oracle.attention_bwd(q, k, v, dO, w.sm_scale, w.causal)
+    return time.perf_counter() - t0
+
+
+def head_flops(w) -> float:
+    f = 4.0 * w.N * w.N * w.d / (2 if w.causal else 1)
+    return f * (3.5 if w.backward else 1.0)
+
+
+def run_reference(args):
+    import oracle
+    from exact_attention_blackwell_gb300 import inputs
+
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    oracle.build()
+    w = workload(args.workload)
+    x = inputs.make_inputs(w, with_dO=w.backward)
+    for s in range(args.warmup):
+        cpu_oracle_step(x, w, s)
+    t = 0.0
+    for s in range(args.steps):
+        t += cpu_oracle_step(x, w, args.warmup + s)
+    value = head_flops(w) * args.steps / t / 1e12
+    cores = oracle.num_threads()
+    sample = f"one (batch, head) slice per step ({w.N} query rows x {w.N} keys, d={w.d}), fwd+bwd, fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name + (" fwd+bwd" if w.backward else " fwd"), "B": w.B, "H": w.H, "Hkv": w.Hkv,
+            "N": w.N, "d": w.d, "causal": w.causal,
+            "l2": "inputs larger than L2 (no flush between steps)", "parallelism": "independent heads per GPU"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    import exact_attention_blackwell_gb300 as fa
+    from exact_attention_blackwell_gb300 import inputs
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local = env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fa.lib()  # fails loudly if the CUDA library is missing
+
+    w = workload(args.workload)
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    scale, causal = w.sm_scale, w.causal
+    xw = inputs.Workload(w.name, B, H, Hkv, N, d, causal, w.seed + 1000 * rank, w.outliers, w.backward)
+    x_cpu = inputs.make_inputs(xw, with_dO=w.backward)
+    dev = torch.device("cuda", local)
+    q, k, v = (x_cpu[n].to(dev) for n in ("q", "k", "v"))
+    dO = x_cpu["dO"].to(dev) if w.backward else None
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def check(st, what):
+        if st != fa.FA_OK:
+            raise fa.FaError(st, what)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    fwd_ev, main_ev = [], []
+
+    def step(record=False):
+        e0, e1 = (ev(), ev()) if record else (None, None)
+        if record:
+            e0.record(stream)
+        check(fa.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, sptr), "fa_fwd")
+        if record:
+            e1.record(stream)
+            fwd_ev.append((e0, e1))
+        if not w.backward:
+            return
+        check(fa.fa_bwd_prepare(o, lse, dO, B, H, Hkv, N, d, ws, ws_bytes, sptr), "fa_bwd_prepare")
+        m0, m1 = (ev(), ev()) if record else (None, None)
+        if record:
+            m0.record(stream)
+        check(fa.fa_bwd_main(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, ws, ws_bytes, sptr),
+              "fa_bwd_main")
+        if record:
+            m1.record(stream)
+            main_ev.append((m0, m1))
+        check(fa.fa_bwd_finish(dq, B, H, Hkv, N, d, scale, ws, ws_bytes, sptr), "fa_bwd_finish")
+
+    launches_per_step = 4 if w.backward else 1
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait during warm-up")
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    if not torch.isfinite(o).all() or (w.backward and not torch.isfinite(dq.float()).all()):
+        raise RuntimeError("non-finite outputs")
+
+    fwd_f = w.fwd_flops()
+    bwd_f = w.bwd_flops() if w.backward else 0.0
+    step_f = fwd_f + bwd_f
+    ms_step = total_ms / args.steps
+    value = world * step_f * args.steps / (total_ms * 1e-3) / 1e12
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    peaks = measured_peaks()
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
+           "config": config_of(w), "frac_of_2250_tflops": value / world / NOMINAL_BF16_TFLOPS,
+           "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms}
+    if w.backward:
+        main_ms = statistics.mean(a.elapsed_time(b) for a, b in main_ev)
+        src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
+        out["bwd_ms"] = ms_step - fwd_ms
+        out["bwd_tflops"] = bwd_f / ((ms_step - fwd_ms) * 1e-3) / 1e12
+        achieved = bwd_f / (main_ms * 1e-3) / 1e12
+        out["roofline"] = {
+            "bound": "tensor", "kernel": "bwd_main_kernel", "achieved": achieved,
+            "peak": peaks["sustained"], "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
+            "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
+            "flops_per_launch": bwd_f, "launch_ms": main_ms,
+            "traffic": profiled_traffic(f"bwd_main_{args.workload}.md", src),
+        }
+    else:
+        src = kernel_source_hash(["fa_fwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
+        achieved = fwd_f / (fwd_ms * 1e-3) / 1e12
+        out["roofline"] = {
+            "bound": "tensor", "kernel": "fa_fwd_kernel", "achieved": achieved, "peak": peaks["sustained"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
+            "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
+            "flops_per_launch": fwd_f, "launch_ms": fwd_ms,
+            "traffic": profiled_traffic(f"fwd_{args.workload}.md", src),
+        }
+    out["gpu_launches"] = launches_per_step * args.steps
+    out["clocks"] = clocks
+
+    # ---- end to end through the C ABI with host buffers: H2D inputs, D2H outputs every step
+    pin = {n: x_cpu[n].pin_memory() for n in ("q", "k", "v") + (("dO",) if w.backward else ())}
+    outs_d = [o, lse] + ([dq, dk, dv] if w.backward else [])
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_d]
+    dsts = {"q": q, "k": k, "v": v, "dO": dO}
+
+    def e2e_step():
+        for n, h in pin.items():
+            dsts[n].copy_(h, non_blocking=True)
+        step()
+        for hd, dd in zip(outs_h, outs_d):
+            hd.copy_(dd, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    out["e2e"] = {"value": world * step_f * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                  "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h),
+                  "ms_per_step": e2e_ms / e2e_steps}
+
+    # ---- CPU oracle on the host cores (rank 0, single GPU only), a bounded sample
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        t = cpu_oracle_step(x_cpu, w, 0)
+        out["cpu_baseline"] = {"value": head_flops(w) / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                               "kind": "oracle", "seconds": t,
+                               "sample": f"(batch 0, head 0) slice: {N} query rows x {N} keys, d={d}, "
+                                         f"{'fwd+bwd' if w.backward else 'fwd'}, fp64"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["headline", "causal", "gqa"], default="headline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, whatever is asked
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -141,43 +141,101 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {
   return up(acc) + 2 * up(rows);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Validation and parameter set-up shared by fa_bwd and its three stages.
+// Pointers passed as nullptr are not needed by the stage and are not checked.
+int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const void *dO, const void *dk,
+              const void *dv, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
+              size_t workspace_bytes, bool maps) {
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  for (const void *x : {q, k, v, dO, dk, dv})
+    if (x && !aligned16(x)) return FA_ERR_ALIGNMENT;
+  const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_WORKSPACE;
+  if ((rc = check_device()) != FA_OK) return rc;
+  std::memset(p, 0, sizeof(*p));
+  if (maps && (encode_bf16_tile_map(&p->tm_q, q, B, N, H, d, 128) ||
+               encode_bf16_tile_map(&p->tm_k, k, B, N, Hkv, d, 128) ||
+               encode_bf16_tile_map(&p->tm_v, v, B, N, Hkv, d, 128) ||
+               encode_bf16_tile_map(&p->tm_do, dO, B, N, H, d, 128) ||
+               encode_bf16_tile_map(&p->tm_dk, dk, B, N, Hkv, d, 128) ||
+               encode_bf16_tile_map(&p->tm_dv, dv, B, N, Hkv, d, 128)))
+    return FA_ERR_CUDA;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t Npad = ((size_t)N + 127) / 128 * 128;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  p->dq_acc = reinterpret_cast<float *>(ws);
+  p->lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
+  p->delta = reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(p->lse2) +
+                                             up((size_t)B * H * Npad * sizeof(float)));
+  p->status = device_status_ptr();
+  if (!p->status) return FA_ERR_CUDA;
+  p->B = B;
+  p->H = H;
+  p->Hkv = Hkv;
+  p->N = N;
+  p->scale = scale;
+  p->scale_log2 = scale * 1.4426950408889634f;
+  return FA_OK;
+}
+
+bool misaligned4(const void *x) { return (reinterpret_cast<uintptr_t>(x) & 3u) != 0; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd_prepare(const void *o, const float *lse, const void *dO, int B, int H, int Hkv, int N, int d,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+  if (!o || !lse || !dO) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
+  BwdParams p;
+  int rc = setup_bwd(&p, nullptr, nullptr, nullptr, dO, nullptr, nullptr, B, H, Hkv, N, d, 1.0f, workspace,
+                     workspace_bytes, false);
+  if (rc != FA_OK) return rc;
+  return launch_bwd_pre(p, d, o, dO, lse, static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_main(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv, int B, int H,
+                int Hkv, int N, int d, float scale, int causal, void *workspace, size_t workspace_bytes,
+                void *stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  BwdParams p;
+  int rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes, true);
+  if (rc != FA_OK) return rc;
+  return launch_bwd_main(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+  if (!dq) return FA_ERR_INVALID_ARG;
+  BwdParams p;
+  int rc = setup_bwd(&p, nullptr, nullptr, nullptr, nullptr, dq, nullptr, B, H, Hkv, N, d, scale, workspace,
+                     workspace_bytes, false);
+  if (rc != FA_OK) return rc;
+  return launch_bwd_post(p, d, dq, static_cast<cudaStream_t>(stream));
+}
+
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
            void *dk, void *dv, int B, int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
            size_t workspace_bytes, void *stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int rc = check_common(B, H, Hkv, N, d, scale);
   if (rc != FA_OK) return rc;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
-      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return FA_ERR_ALIGNMENT;
-  const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return FA_ERR_WORKSPACE;
-  if ((rc = check_device()) != FA_OK) return rc;
+  if (!aligned16(o) || !aligned16(dq) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
   BwdParams p;
-  std::memset(&p, 0, sizeof(p));
-  if (encode_bf16_tile_map(&p.tm_q, q, B, N, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
-      encode_bf16_tile_map(&p.tm_v, v, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_do, dO, B, N, H, d, 128) ||
-      encode_bf16_tile_map(&p.tm_dk, dk, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_dv, dv, B, N, Hkv, d, 128))
-    return FA_ERR_CUDA;
-  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  float *dq_acc = reinterpret_cast<float *>(ws);
-  float *lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
-  const size_t Npad = ((size_t)N + 127) / 128 * 128;
-  float *delta = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(lse2) + up((size_t)B * H * Npad * sizeof(float)));
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.dq_acc = dq_acc;
-  p.status = device_status_ptr();
-  if (!p.status) return FA_ERR_CUDA;
-  p.B = B;
-  p.H = H;
-  p.Hkv = Hkv;
-  p.N = N;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  return launch_bwd(p, d, causal != 0, o, dO, lse, dq, lse2, delta, static_cast<cudaStream_t>(stream));
+  if ((rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes, true)) != FA_OK)
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
+  if ((rc = launch_bwd_main(p, d, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_post(p, d, dq, s);
 }
 
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {

@@ -478,31 +478,39 @@ int launch_main(const BwdParams &p, cudaStream_t stream) {
 }
 
 template <int D>
-int launch_all(const BwdParams &p, bool causal, const void *o, const void *dO, const float *lse, void *dq,
-               float *lse2, float *delta, cudaStream_t stream) {
+int launch_pre_t(const BwdParams &p, const void *o, const void *dO, const float *lse, cudaStream_t stream) {
   const int Npad = (p.N + 127) / 128 * 128;
   const long long rows = (long long)p.B * Npad * p.H;
   bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, lse2, delta, p.dq_acc,
-      p.B, p.H, p.N, Npad);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const int rc = causal ? launch_main<D, true>(p, stream) : launch_main<D, false>(p, stream);
-  if (rc != FA_OK) return rc;
-  const long long n8 = (long long)p.B * p.N * p.H * D / 8;
-  bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16 *>(dq), n8,
-                                                                     p.scale);
+      static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, p.lse2,
+      const_cast<float *>(p.delta), p.dq_acc, p.B, p.H, p.N, Npad);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_bwd(const BwdParams &p, int d, bool causal, const void *o, const void *dO, const float *lse, void *dq,
-               float *lse2, float *delta, cudaStream_t stream) {
+int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, const float *lse, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_all<64>(p, causal, o, dO, lse, dq, lse2, delta, stream);
-    case 128: return launch_all<128>(p, causal, o, dO, lse, dq, lse2, delta, stream);
+    case 64: return launch_pre_t<64>(p, o, dO, lse, stream);
+    case 128: return launch_pre_t<128>(p, o, dO, lse, stream);
     default: return FA_ERR_UNSUPPORTED;
   }
+}
+
+int launch_bwd_main(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
+  switch (d) {
+    case 64: return causal ? launch_main<64, true>(p, stream) : launch_main<64, false>(p, stream);
+    case 128: return causal ? launch_main<128, true>(p, stream) : launch_main<128, false>(p, stream);
+    default: return FA_ERR_UNSUPPORTED;
+  }
+}
+
+int launch_bwd_post(const BwdParams &p, int d, void *dq, cudaStream_t stream) {
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long n8 = (long long)p.B * p.N * p.H * d / 8;
+  bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16 *>(dq), n8,
+                                                                     p.scale);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace fa

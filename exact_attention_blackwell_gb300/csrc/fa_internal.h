@@ -37,8 +37,8 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
   CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
-  const float *lse2;                    // [B, H, N] LSE * log2(e)
-  const float *delta;                   // [B, H, N] D = rowsum(dO * O)
+  float *lse2;                          // [B, H, Npad] LSE * log2(e)
+  const float *delta;                   // [B, H, Npad] D = rowsum(dO * O)
   float *dq_acc;                        // [B, N, H, d] fp32 accumulator
   unsigned *status;
   int B, H, Hkv, N;
@@ -54,7 +54,9 @@ unsigned *device_status_ptr();
 int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows);
 
 int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream);
-int launch_bwd(const BwdParams &p, int d, bool causal, const void *o, const void *dO, const float *lse,
-               void *dq, float *lse2_ws, float *delta_ws, cudaStream_t stream);
+// The three launches of the backward pass (fa_bwd runs them in this order).
+int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, const float *lse, cudaStream_t stream);
+int launch_bwd_main(const BwdParams &p, int d, bool causal, cudaStream_t stream);
+int launch_bwd_post(const BwdParams &p, int d, void *dq, cudaStream_t stream);
 
 }  // namespace fa

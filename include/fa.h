@@ -72,7 +72,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse from the forward, and dO [B,N,H,d].
- * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  `workspace` is caller
+ * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  Head dims 64 and 128
+ * (d = 256 returns FA_ERR_UNSUPPORTED).  `workspace` is caller
  * owned device memory of at least fa_bwd_workspace_bytes() bytes, 256-byte
  * aligned; its contents on entry do not matter and are overwritten.  The call
  * is not deterministic in the last bits (dQ is summed with atomics). */
@@ -80,6 +81,22 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dO, void *dq, void *dk, void *dv,
            int B, int H, int Hkv, int N, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
+
+/* The three launches fa_bwd makes, for callers that schedule them separately
+ * (same arguments and rules as fa_bwd; run them in this order on one stream,
+ * with the same workspace):
+ *   fa_bwd_prepare: D = rowsum(dO * O) and the log2-scaled LSE into the
+ *                   workspace, the dQ accumulator zeroed (memory bound);
+ *   fa_bwd_main:    the fused kernel: recomputes P from LSE, writes dk and dv,
+ *                   accumulates dQ in the workspace;
+ *   fa_bwd_finish:  dq = bf16(scale * accumulator). */
+int fa_bwd_prepare(const void *o, const float *lse, const void *dO, int B, int H, int Hkv, int N, int d,
+                   void *workspace, size_t workspace_bytes, void *stream);
+int fa_bwd_main(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv,
+                int B, int H, int Hkv, int N, int d, float scale, int causal,
+                void *workspace, size_t workspace_bytes, void *stream);
+int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale,
+                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* The software 2^x the forward kernel evaluates on the FMA pipe (FlashAttention-4
  * paper summary, section 2.B: 2^x emulated with FMA instructions, a polynomial

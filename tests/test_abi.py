@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_exp2_poly", "fa_last_device_status",
-              "fa_status_string"):
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish",
+              "fa_exp2_poly", "fa_last_device_status", "fa_status_string"):
         assert n in names
 
 
@@ -88,6 +88,19 @@ def test_bwd_rejects_bad_arguments(lib, args, code):
     wsb = nbytes if a["ws_bytes"] is None else a["ws_bytes"]
     assert fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dO"], a["dq"], a["dk"], a["dv"], a["B"],
                      a["H"], a["Hkv"], a["N"], a["d"], a["scale"], a["causal"], a["ws"], wsb, 0) == code
+
+
+def test_bwd_stages_reject_bad_arguments(lib):
+    nb = fa.fa_bwd_workspace_bytes(1, 2, 2, 256, 128)
+    assert fa.fa_bwd_prepare(None, A, A, 1, 2, 2, 256, 128, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_prepare(A, A + 2, A, 1, 2, 2, 256, 128, A, nb, 0) == fa.FA_ERR_ALIGNMENT
+    assert fa.fa_bwd_prepare(A, A, A, 1, 2, 2, 256, 128, A, nb - 4, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd_main(A, A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_main(A, A, A, A, A, A, 1, 2, 2, 256, 256, 0.1, 0, A, nb, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_main(A, A, A, A, A + 8, A, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_ALIGNMENT
+    assert fa.fa_bwd_finish(None, 1, 2, 2, 256, 128, 0.1, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_finish(A, 1, 2, 2, 256, 128, -0.1, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_finish(A, 1, 2, 2, 256, 128, 0.1, None, nb, 0) == fa.FA_ERR_WORKSPACE
 
 
 def test_workspace_size():

@@ -24,13 +24,26 @@ def run(q, k, v, dO, scale, causal):
 
 
 def check_all(got, ref, what):
+    """Relative L2 per tensor (the target, 1e-2), plus the same measure per
+    128-row tile of each (batch, head) so that one wrong tile cannot hide in a
+    whole-tensor norm.  The tile bound is 3e-2, its denominator floored at a
+    tenth of the typical tile norm (a tile whose exact gradient nearly cancels,
+    e.g. one-hot softmax rows where dP_ij ~ D_i, carries the bf16 rounding of
+    O in D = rowsum(dO * O) without a matching signal)."""
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         check_grad(g, r, f"{what} {name}")
+        if np.linalg.norm(r) == 0.0:
+            continue
         gg = g.float().numpy().astype(np.float64)
-        # no element may be far off either: 5% of the tensor's RMS plus bf16 rounding
-        bound = 0.05 * np.sqrt((r ** 2).mean()) + np.abs(r) * 2.0 ** -7
-        err = np.abs(gg - r)
-        assert (err <= bound).all(), f"{what} {name}: worst element error {err.max():.3e}"
+        B, N, Hx, d = r.shape
+        pad = (-N) % 128
+        e = np.pad(gg - r, ((0, 0), (0, pad), (0, 0), (0, 0))).reshape(B, -1, 128, Hx, d)
+        rr = np.pad(r, ((0, 0), (0, pad), (0, 0), (0, 0))).reshape(B, -1, 128, Hx, d)
+        err_t = np.sqrt((e ** 2).sum(axis=(2, 4)))
+        ref_t = np.sqrt((rr ** 2).sum(axis=(2, 4)))
+        floor = 0.1 * np.sqrt((ref_t ** 2).mean())
+        rel = err_t / np.maximum(ref_t, floor)
+        assert (rel <= 3e-2).all(), f"{what} {name}: tile (b, tile, head) {np.unravel_index(rel.argmax(), rel.shape)} rel {rel.max():.3e}"
 
 
 def test_tiny_workload_full(oracle_mod):
