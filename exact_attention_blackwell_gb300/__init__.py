@@ -33,6 +33,7 @@ SIGNATURES = {
     "fa_bwd_prepare": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_finish": (_I, [_P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_exp2_poly": (_I, [_P, _P, _LL, _P]),
     "fa_last_device_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -116,6 +117,16 @@ def fa_bwd_main(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, 
 def fa_bwd_finish(dq, B, H, Hkv, N, d, scale, workspace, workspace_bytes, stream=None) -> int:
     return lib().fa_bwd_finish(_ptr(dq), B, H, Hkv, N, d, float(scale), _ptr(workspace), int(workspace_bytes),
                                _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
+    """fa_bwd without a workspace: for callers that cannot allocate device
+    memory when they run the backward pass (see include/fa.h)."""
+    return lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, H, Hkv, N, d, float(scale), int(bool(causal)), _stream(stream))
+
+
+FA_BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def fa_exp2_poly(x, y, n, stream=None) -> int:

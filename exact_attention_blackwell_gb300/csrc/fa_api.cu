@@ -238,6 +238,68 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   return launch_bwd_post(p, d, dq, s);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free backward
+// Some callers cannot allocate device memory when they run the backward pass:
+// plug-ins living inside a host framework that owns every device allocation
+// through its own pool, and serving or training loops that forbid cudaMalloc
+// after start-up because it synchronises the device and fragments memory.
+// fa_bwd_noalloc serves them: its scratch (the fp32 dQ accumulator and the
+// per-row D / log2-LSE terms that fa_bwd keeps in the caller's workspace) is
+// this file-scope device array instead.  Every GPU that loads the library holds
+// it until the process exits.
+namespace fa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = FA_BWD_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device.  In host code the
+// array's name only stands for it; the address is looked up once per device,
+// with that device current, and cached.
+int scratch_address(void **out) {
+  int dev;
+  if (current_device(&dev) != FA_OK) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || ptr == nullptr) return FA_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                   void *stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(o) || !aligned16(dq) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
+  const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
+  if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;  // problem too large for the built-in scratch
+  void *ws = nullptr;
+  if ((rc = scratch_address(&ws)) != FA_OK) return rc;
+  BwdParams p;
+  if ((rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, ws, kNoAllocScratchBytes, true)) != FA_OK)
+    return rc;
+  // bwd_pre writes every part of the scratch that the other launches read
+  // (zeroes the accumulator, fills D and log2-LSE), so stale contents left by
+  // an earlier call do not matter.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
+  if ((rc = launch_bwd_main(p, d, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_post(p, d, dq, s);
+}
+
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {
   if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u)) return FA_ERR_ALIGNMENT;

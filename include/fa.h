@@ -98,6 +98,31 @@ int fa_bwd_main(const void *q, const void *k, const void *v, const void *dO, voi
 int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward pass that allocates nothing and takes no workspace.  The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory at the time they run the backward pass (a plug-in inside a host
+ * framework that owns all device memory through its own pool; a serving or
+ * training loop that forbids cudaMalloc after start-up, since it synchronises
+ * the device and fragments memory).  Same arguments, results and rules as
+ * fa_bwd, except that the scratch fa_bwd keeps in the caller's workspace lives
+ * in one static device array of FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *   - Sizes whose fa_bwd_workspace_bytes() exceeds FA_BWD_NOALLOC_SCRATCH_BYTES
+ *     are rejected with FA_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU
+ *     (different streams, or different host threads, without ordering between
+ *     them) race and corrupt each other's results.  Each call re-initialises
+ *     what it reads, so the contents a previous call left do not matter.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dO, void *dq, void *dk, void *dv,
+                   int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
+
 /* The software 2^x the forward kernel evaluates on the FMA pipe (FlashAttention-4
  * paper summary, section 2.B: 2^x emulated with FMA instructions, a polynomial
  * of degree 3 to 5 for the fractional part).  Range reduction x = j + f with
