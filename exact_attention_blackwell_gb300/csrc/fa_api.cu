@@ -70,6 +70,34 @@ unsigned *device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+namespace {
+int get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return FA_OK;
+}
+}  // namespace
+
+int encode_f32_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows) {
+  if (get_encoder() != FA_OK) return FA_ERR_CUDA;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hx, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)Hx * d * 4, (cuuint64_t)N * Hx * d * 4};
+  const cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -171,6 +199,7 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
   const size_t Npad = ((size_t)N + 127) / 128 * 128;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p->dq_acc = reinterpret_cast<float *>(ws);
+  if (maps && encode_f32_tile_map(&p->tm_dqacc, p->dq_acc, B, N, H, d, 128)) return FA_ERR_CUDA;
   p->lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
   p->delta = reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(p->lse2) +
                                              up((size_t)B * H * Npad * sizeof(float)));

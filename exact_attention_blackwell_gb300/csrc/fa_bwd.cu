@@ -111,19 +111,18 @@ template <int D>
 struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kStages = 2;          // (Q_i, dO_i, LSE2_i, D_i) ring depth
-  static constexpr int kThreads = 320;
-  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  static constexpr int kThreads = 448;
+  static constexpr int kDrainWarp0 = 8, kMmaWarp = 12, kLoadWarp = 13;
   static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kTmemCols = 512;
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffStage = 2 * kTile;      // stage s: Q at +2s*kTile, dO at +(2s+1)*kTile
-  static constexpr int kOffDS = kOffStage + 2 * kStages * kTile;  // dS^T, 128 x 128 bf16
+  static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +2s*kTile, dO at +(2s+1)*kTile
+  static constexpr int kOffDS = kOffStage + 2 * kStages * kTile;  // dS^T 128 x 128 bf16; also dQ staging
   static constexpr int kOffRows = kOffDS + 128 * 128 * 2;          // stage s: LSE2 at +1024s, D at +1024s+512
-  // barriers
   enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarS = kBarEmpty0 + kStages, kBarDP, kBarP, kBarDS,
-         kBarDSFree, kBarDQFull, kBarDQEmpty, kBarFinal, kBarDrain, kNumBars };
+         kBarDQFull, kBarDQEmpty, kBarStageFree, kBarFinal, kBarDrain, kNumBars };
   static constexpr int kOffBar = kOffRows + 1024 * kStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked in the kernel)
@@ -132,11 +131,11 @@ struct BwdCfg {
 
 enum BwdSite : int {
   kBSiteKV = 11, kBSiteFull = 12, kBSiteEmpty = 13, kBSiteS = 14, kBSiteDP = 15, kBSiteP = 16, kBSiteDS = 17,
-  kBSiteDSFree = 18, kBSiteDQFull = 19, kBSiteDQEmpty = 20, kBSiteFinal = 21, kBSiteDrain = 22, kBSiteAlign = 23
+  kBSiteStageFree = 18, kBSiteDQFull = 19, kBSiteDQEmpty = 20, kBSiteFinal = 21, kBSiteDrain = 22, kBSiteAlign = 23
 };
 
-// Writes 32 packed bf16 pairs (64 columns) -- here 16 words = 32 columns -- of
-// row r into a 128B-swizzled [rows][128 cols] tile made of two 64-column boxes.
+// Writes 16 packed bf16 pairs (32 columns starting at col0) of row r into a
+// 128B-swizzled bf16 tile made of 64-column boxes of 128 rows (16 KB each).
 __device__ __forceinline__ void st_swizzled_32cols(uint8_t *tile, int r, int col0, const uint32_t (&w)[16]) {
   const int box = col0 >> 6;
   const int chunk0 = (col0 & 63) >> 3;
@@ -148,8 +147,24 @@ __device__ __forceinline__ void st_swizzled_32cols(uint8_t *tile, int r, int col
   }
 }
 
+// Writes 32 fp32 of row r into one 128B-swizzled fp32 box (32 columns x 128 rows, 16 KB).
+__device__ __forceinline__ void st_swizzled_f32_box(uint8_t *box, int r, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int chunk = k ^ (r & 7);
+    *reinterpret_cast<uint4 *>(box + r * 128 + chunk * 16) = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+}
+
+__device__ __forceinline__ void tma_reduce_add_4d(const void *map, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -179,8 +194,12 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
   const int kv0 = jt * 128;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarP || i == C::kBarDS || i == C::kBarDQEmpty) ? 128u : 1u);
+    for (int i = 0; i < C::kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i == C::kBarP || i == C::kBarDS) count = 256;  // both P/dS warpgroups
+      if (i == C::kBarDQEmpty) count = 128;              // the drain warpgroup
+      mbar_init(bar(i), count);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -193,18 +212,21 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_dqacc);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
-    // ===================================================== P^T and dS^T (row = key row)
-    const int r = threadIdx.x;  // 0..127
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + C::kColS;
-    const uint32_t dp_tm = tmem + lane_off + C::kColDP;
+  if (warp < 8) {
+    // ===================================================== P^T and dS^T, one warpgroup per 64 query columns
+    const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
+    const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;   // this warpgroup's S^T columns
+    const uint32_t p_tm = s_tm;                                   // P^T (bf16) over their first 32
+    const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
     const int kv_row = kv0 + r;
     const bool row_valid = kv_row < p.N;
     uint8_t *ds_tile = smem + C::kOffDS;
@@ -212,149 +234,146 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
     for (int it = 0; it < n_iter && ok; ++it) {
       const int st = it % C::kStages;
       const int i = i_start + it % per_head;
-      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * st);
+      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * st) + 64 * wg;
       const float *dlt_s = lse2_s + 128;
       // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
       ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
       if (!ok) break;
       tc_fence_after();
       const bool diag = CAUSAL && (i == jt);
+      uint32_t sv[2][32];
+      tmem_ld_32x32b_x32(s_tm, sv[0]);
+      tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+      tmem_wait_ld(sv[0]);
+      reg_tie(sv[1]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(s_tm + 32 * c, sv);
-        tmem_wait_ld(sv);
+      for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + (k & ~3));
-          const float la = (k & 3) ? l4.z : l4.x, lb = (k & 3) ? l4.w : l4.y;
-          float pa = ex2_mufu(fmaf(__uint_as_float(sv[k]), p.scale_log2, -la));
-          float pb = ex2_mufu(fmaf(__uint_as_float(sv[k + 1]), p.scale_log2, -lb));
-          const int qc = 32 * c + k;  // query column within tile i
-          if (!row_valid || (diag && qc < r)) pa = 0.f;
-          if (!row_valid || (diag && qc + 1 < r)) pb = 0.f;
-          w[k >> 1] = pack_bf16x2(pa, pb);
+        for (int k = 0; k < 32; k += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
+          float pe[4];
+          pe[0] = ex2_mufu(fmaf(__uint_as_float(sv[c][k]), p.scale_log2, -l4.x));
+          pe[1] = ex2_mufu(fmaf(__uint_as_float(sv[c][k + 1]), p.scale_log2, -l4.y));
+          pe[2] = ex2_mufu(fmaf(__uint_as_float(sv[c][k + 2]), p.scale_log2, -l4.z));
+          pe[3] = ex2_mufu(fmaf(__uint_as_float(sv[c][k + 3]), p.scale_log2, -l4.w));
+          const int qc = 64 * wg + 32 * c + k;  // query column within tile i
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (!row_valid || (diag && qc + u < r)) pe[u] = 0.f;
+          w[k >> 1] = pack_bf16x2(pe[0], pe[1]);
+          w[(k >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
         }
-        tmem_st_32x32b_x16(s_tm + 16 * c, w);
+        tmem_st_32x32b_x16(p_tm + 16 * c, w);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarP));
-      // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, 128B swizzle)
+      // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, 128B swizzle, box = wg)
       ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
-      if (ok && it > 0) ok = mbar_wait_warp(bar(C::kBarDSFree), (it - 1) & 1, wctx, kBSiteDSFree);
+      if (ok && it > 0) ok = mbar_wait_warp(bar(C::kBarStageFree), (it - 1) & 1, wctx, kBSiteStageFree);
       if (!ok) break;
       tc_fence_after();
+      uint32_t dpv[2][32], pv[32];
+      tmem_ld_32x32b_x32(dp_tm, dpv[0]);
+      tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
+      tmem_ld_32x32b_x32(p_tm, pv);
+      tmem_wait_ld(dpv[0]);
+      reg_tie(dpv[1]);
+      reg_tie(pv);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dpv[32], pv[16];
-        tmem_ld_32x32b_x32(dp_tm + 32 * c, dpv);
-        tmem_ld_32x32b_x16(s_tm + 16 * c, pv);
-        tmem_wait_ld(dpv);
-        tmem_wait_ld(pv);
+      for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
           const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + 32 * c + k);
-          const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[k >> 1]);
-          const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[(k >> 1) + 1]);
-          const float ds0 = __low2float(p01) * (__uint_as_float(dpv[k]) - d4.x);
-          const float ds1 = __high2float(p01) * (__uint_as_float(dpv[k + 1]) - d4.y);
-          const float ds2 = __low2float(p23) * (__uint_as_float(dpv[k + 2]) - d4.z);
-          const float ds3 = __high2float(p23) * (__uint_as_float(dpv[k + 3]) - d4.w);
+          const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[16 * c + (k >> 1)]);
+          const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[16 * c + (k >> 1) + 1]);
+          const float ds0 = __low2float(p01) * (__uint_as_float(dpv[c][k]) - d4.x);
+          const float ds1 = __high2float(p01) * (__uint_as_float(dpv[c][k + 1]) - d4.y);
+          const float ds2 = __low2float(p23) * (__uint_as_float(dpv[c][k + 2]) - d4.z);
+          const float ds3 = __high2float(p23) * (__uint_as_float(dpv[c][k + 3]) - d4.w);
           w[k >> 1] = pack_bf16x2(ds0, ds1);
           w[(k >> 1) + 1] = pack_bf16x2(ds2, ds3);
         }
-        st_swizzled_32cols(ds_tile, r, 32 * c, w);
+        st_swizzled_32cols(ds_tile, r, 64 * wg + 32 * c, w);
       }
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       tc_fence_before();
       mbar_arrive(bar(C::kBarDS));
     }
-    // ---- epilogue: dV -> bf16 -> shared (stage 0, Q slot) -> TMA store
+    // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via stage 0's Q / dO slots)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
-    uint8_t *stage = smem + C::kOffStage;
+    uint8_t *stage = smem + C::kOffStage + wg * C::kTile;
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
     if (ok) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::kColDV + 32 * c, v);
-        tmem_wait_ld(v);
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-        st_swizzled_32cols(stage, r, 32 * c, w);
-      }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (r == 0 && ok) {
-      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(&p.tm_dv, sbase + C::kOffStage + bx * 16384, bx * 64, kh, kv0, b);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
-  } else if (warp < 8) {
-    // ===================================================== dQ drain, dK epilogue (row = query row)
-    const int r = threadIdx.x - 128;
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const uint32_t dq_tm = tmem + lane_off + C::kColDP;
-    bool ok = true;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const int hh = kh * g + it / per_head;
-      const int i = i_start + it % per_head;
-      const int q_row = i * 128 + r;
-      ok = mbar_wait_warp(bar(C::kBarDQFull), it & 1, wctx, kBSiteDQFull);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32(dq_tm + 32 * c, v[c]);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (c == 0) tmem_wait_ld(v[0]);
-        else reg_tie(v[c]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDQEmpty));
-      if (q_row < p.N) {
-        float *dst = p.dq_acc + (((size_t)b * p.N + q_row) * p.H + hh) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 32 * c + k), "f"(__uint_as_float(v[c][k])),
-                         "f"(__uint_as_float(v[c][k + 1])), "f"(__uint_as_float(v[c][k + 2])),
-                         "f"(__uint_as_float(v[c][k + 3]))
-                         : "memory");
-      }
-    }
-    // ---- epilogue: dK * scale -> bf16 -> shared (stage 0, dO slot) -> TMA store
-    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
-    tc_fence_after();
-    uint8_t *stage = smem + C::kOffStage + C::kTile;
-    if (ok) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::kColDK + 32 * c, v);
+        tmem_ld_32x32b_x32(acc_tm + 32 * c, v);
         tmem_wait_ld(v);
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          w[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * p.scale, __uint_as_float(v[2 * k + 1]) * p.scale);
+          w[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
         st_swizzled_32cols(stage, r, 32 * c, w);
       }
     }
     fence_proxy_async_smem();
-    named_bar_sync(2, 128);
+    if (wg == 0) named_bar_sync(1, 128);
+    else named_bar_sync(2, 128);
     if (r == 0 && ok) {
-      for (int bx = 0; bx < D / 64; ++bx)
-        tma_store_4d(&p.tm_dk, sbase + C::kOffStage + C::kTile + bx * 16384, bx * 64, kh, kv0, b);
+      const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, kv0, b);
       bulk_commit();
       bulk_wait_read_all();
     }
+  } else if (warp < C::kMmaWarp) {
+    // ===================================================== dQ drain: TMEM -> staging (dS tile) -> TMA reduce-add
+    const int r = threadIdx.x - 256;  // query row within tile i == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp - C::kDrainWarp0) * 32) << 16;
+    const uint32_t dq_tm = tmem + lane_off + C::kColDP;
+    uint8_t *staging = smem + C::kOffDS;  // free from dQ_i's completion until dS_{i+1} is written
+    // Every thread of this warpgroup runs every iteration (and every named
+    // barrier in it), also after an abort, so the barriers always match; waits
+    // return at once once the abort flag is set.
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int hh = kh * g + it / per_head;
+      const int i = i_start + it % per_head;
+      if (ok) ok = mbar_wait_warp(bar(C::kBarDQFull), it & 1, wctx, kBSiteDQFull);
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t v[2][32];
+        if (ok) {
+          tmem_ld_32x32b_x32(dq_tm + 64 * half, v[0]);
+          tmem_ld_32x32b_x32(dq_tm + 64 * half + 32, v[1]);
+          tmem_wait_ld(v[0]);
+          reg_tie(v[1]);
+          if (half == D / 64 - 1) {  // every TMEM read of dQ_i done: dP^T_{i+1} may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarDQEmpty));
+          }
+          st_swizzled_f32_box(staging, r, v[0]);
+          st_swizzled_f32_box(staging + 16384, r, v[1]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(3, 128);
+        if (r == 0 && !*abort_flag) {
+          const uint32_t src = smem_u32(staging);
+          tma_reduce_add_4d(&p.tm_dqacc, src, 64 * half, hh, i * 128, b);
+          tma_reduce_add_4d(&p.tm_dqacc, src + 16384, 64 * half + 32, hh, i * 128, b);
+          bulk_commit();
+          bulk_wait_read_all();  // staging may be overwritten once the copies have read it
+        }
+        named_bar_sync(3, 128);
+      }
+      if (r == 0) mbar_arrive(bar(C::kBarStageFree));
+    }
+    if (threadIdx.x == 256) bulk_wait_all();  // reductions complete before the CTA exits
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
     if (lane == 0) {
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
                  kk > 0);
         }
         tc_commit(bar(C::kBarS));
-        // dP^T = V dO^T  (into the dP columns: dQ_{i-1} must have been drained)
+        // dP^T = V dO^T  (into the dP columns: dQ_{i-1} must have been read out)
         if (it > 0) ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, wctx, kBSiteDQEmpty);
         if (!ok) break;
         tc_fence_after();
@@ -388,14 +407,14 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
                  id_kk, kk > 0);
         }
         tc_commit(bar(C::kBarDP));
-        // dV += P^T dO   (A = P^T in TMEM, 8 columns per 16 query rows; B = dO MN-major)
+        // dV += P^T dO   (A = P^T in TMEM: query columns 64w..64w+63 at column 64w, two bf16 per column)
         ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + 8u * kk, make_sdesc_sw128(do_s + kk * 2048, 16384, 1024), id_dv,
-                 (it > 0 || kk > 0));
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + 64u * (kk >> 2) + 8u * (kk & 3),
+                 make_sdesc_sw128(do_s + kk * 2048, 16384, 1024), id_dv, (it > 0 || kk > 0));
         // dK += dS^T Q  (A = dS^T K-major [key][query]; B = Q MN-major)
         ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
@@ -412,7 +431,6 @@ __global__ void __launch_bounds__(320, 1) bwd_main_kernel(const __grid_constant_
           mma_ss(tmem + C::kColDP, make_sdesc_sw128(ds_s + kk * 2048, 16384, 1024),
                  make_sdesc_sw128(k_s + kk * 2048, 16384, 1024), id_dq, kk > 0);
         tc_commit(bar(C::kBarDQFull));
-        tc_commit(bar(C::kBarDSFree));
         tc_commit(bar(C::kBarEmpty0 + st));
       }
       tc_commit(bar(C::kBarFinal));
