@@ -38,6 +38,25 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Opt-in event trace (build with -DFA_TRACE): SM clock at fixed points of the
+// first 64 iterations of one CTA, read back with fa_debug_trace().  Off by
+// default; the macro then expands to nothing.
+#ifdef FA_TRACE
+#ifndef FA_TRACE_CTA
+#define FA_TRACE_CTA 7
+#endif
+__device__ unsigned long long g_trace[64][16];
+#define FA_TRACE_EV(it, ev)                                                                      \
+  do {                                                                                           \
+    if (blockIdx.x == FA_TRACE_CTA && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 64)           \
+      g_trace[(it)][(ev)] = clock64();                                                           \
+  } while (0)
+#else
+#define FA_TRACE_EV(it, ev) \
+  do {                      \
+  } while (0)
+#endif
+
 // ------------------------------------------------------------------ pre / post
 template <int E> struct BfVec;  // E bf16 values loaded at once
 template <> struct BfVec<2> { using T = uint32_t; };
@@ -192,6 +211,11 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
   const int per_head = n_q - i_start;
   const int n_iter = g * per_head;  // (head, query tile) pairs, head-major
   const int kv0 = jt * 128;
+  // Each key tile walks the query tiles from a different starting point, so
+  // that the CTAs of one head, which run together, reduce into different dQ
+  // rows at any moment instead of all into the same ones.
+  const int rot = (int)(((unsigned)jt * 2654435761u) % (unsigned)per_head);
+  auto q_tile = [&](int it) { return i_start + (it % per_head + rot) % per_head; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
@@ -233,12 +257,13 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int st = it % C::kStages;
-      const int i = i_start + it % per_head;
+      const int i = q_tile(it);
       const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * st) + 64 * wg;
       const float *dlt_s = lse2_s + 128;
       // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
       ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
       if (!ok) break;
+      if (threadIdx.x == 0) FA_TRACE_EV(it, 0);
       tc_fence_after();
       const bool diag = CAUSAL && (i == jt);
       uint32_t sv[2][32];
@@ -269,10 +294,13 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarP));
+      if (threadIdx.x == 0) FA_TRACE_EV(it, 1);
       // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, 128B swizzle, box = wg)
       ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
+      if (threadIdx.x == 0) FA_TRACE_EV(it, 2);
       if (ok && it > 0) ok = mbar_wait_warp(bar(C::kBarStageFree), (it - 1) & 1, wctx, kBSiteStageFree);
       if (!ok) break;
+      if (threadIdx.x == 0) FA_TRACE_EV(it, 3);
       tc_fence_after();
       uint32_t dpv[2][32], pv[32];
       tmem_ld_32x32b_x32(dp_tm, dpv[0]);
@@ -301,6 +329,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       tc_fence_before();
       mbar_arrive(bar(C::kBarDS));
+      if (threadIdx.x == 0) FA_TRACE_EV(it, 4);
     }
     // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via stage 0's Q / dO slots)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
@@ -342,8 +371,9 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int hh = kh * g + it / per_head;
-      const int i = i_start + it % per_head;
+      const int i = q_tile(it);
       if (ok) ok = mbar_wait_warp(bar(C::kBarDQFull), it & 1, wctx, kBSiteDQFull);
+      if (r == 0) FA_TRACE_EV(it, 5);
       tc_fence_after();
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
@@ -368,10 +398,12 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
           tma_reduce_add_4d(&p.tm_dqacc, src + 16384, 64 * half + 32, hh, i * 128, b);
           bulk_commit();
           bulk_wait_read_all();  // staging may be overwritten once the copies have read it
+          FA_TRACE_EV(it, 12 + half);
         }
         named_bar_sync(3, 128);
       }
       if (r == 0) mbar_arrive(bar(C::kBarStageFree));
+      if (r == 0) FA_TRACE_EV(it, 6);
     }
     if (threadIdx.x == 256) bulk_wait_all();  // reductions complete before the CTA exits
   } else if (warp == C::kMmaWarp) {
@@ -387,6 +419,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
         const uint32_t q_s = sbase + C::kOffStage + 2 * st * C::kTile, do_s = q_s + C::kTile;
         ok = mbar_wait(bar(C::kBarFull0 + st), (it / C::kStages) & 1, wctx, kBSiteFull);
         if (!ok) break;
+        FA_TRACE_EV(it, 7);
         tc_fence_after();
         // S^T = K Q^T   (both K-major, K dim = d)
 #pragma unroll
@@ -399,6 +432,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
         // dP^T = V dO^T  (into the dP columns: dQ_{i-1} must have been read out)
         if (it > 0) ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, wctx, kBSiteDQEmpty);
         if (!ok) break;
+        FA_TRACE_EV(it, 8);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -410,6 +444,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
         // dV += P^T dO   (A = P^T in TMEM: query columns 64w..64w+63 at column 64w, two bf16 per column)
         ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
         if (!ok) break;
+        FA_TRACE_EV(it, 9);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -418,6 +453,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
         // dK += dS^T Q  (A = dS^T K-major [key][query]; B = Q MN-major)
         ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
+        FA_TRACE_EV(it, 10);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -432,6 +468,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
                  make_sdesc_sw128(k_s + kk * 2048, 16384, 1024), id_dq, kk > 0);
         tc_commit(bar(C::kBarDQFull));
         tc_commit(bar(C::kBarEmpty0 + st));
+        FA_TRACE_EV(it, 11);
       }
       tc_commit(bar(C::kBarFinal));
       tc_commit(bar(C::kBarDrain));
@@ -454,7 +491,7 @@ __global__ void __launch_bounds__(448, 1) bwd_main_kernel(const __grid_constant_
       for (; it < n_iter && ok; ++it) {
         const int st = it % C::kStages;
         const int hh = kh * g + it / per_head;
-        const int i = i_start + it % per_head;
+        const int i = q_tile(it);
         ok = mbar_wait(bar(C::kBarEmpty0 + st), ((it / C::kStages) & 1) ^ 1, wctx, kBSiteEmpty);
         if (!ok) break;
         const uint32_t fb = bar(C::kBarFull0 + st);
@@ -532,3 +569,9 @@ int launch_bwd_post(const BwdParams &p, int d, void *dq, cudaStream_t stream) {
 }
 
 }  // namespace fa
+
+#ifdef FA_TRACE
+extern "C" int fa_debug_trace(unsigned long long *host_out) {
+  return cudaMemcpyFromSymbol(host_out, fa::g_trace, sizeof(fa::g_trace)) == cudaSuccess ? 0 : -5;
+}
+#endif

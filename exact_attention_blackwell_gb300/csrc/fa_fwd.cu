@@ -35,6 +35,24 @@
 namespace fa {
 namespace {
 
+// Opt-in event trace (build with -DFA_TRACE): SM clock at fixed points of the
+// first 64 key blocks of one CTA, read back with fa_debug_trace_fwd().
+#ifdef FA_TRACE
+#ifndef FA_TRACE_CTA
+#define FA_TRACE_CTA 7
+#endif
+__device__ unsigned long long g_trace_fwd[64][16];
+#define FA_TRACE_EV(j, ev)                                                                       \
+  do {                                                                                           \
+    if (blockIdx.x == FA_TRACE_CTA && blockIdx.y == 0 && blockIdx.z == 0 && (j) < 64)            \
+      g_trace_fwd[(j)][(ev)] = clock64();                                                        \
+  } while (0)
+#else
+#define FA_TRACE_EV(j, ev) \
+  do {                     \
+  } while (0)
+#endif
+
 template <int D>
 struct FwdCfg {
   static constexpr int kQT = (D <= 128) ? 2 : 1;  // query tiles per CTA
@@ -141,6 +159,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
     for (int j = 0; j < nb[t] && ok; ++j) {
       ok = mbar_wait_warp(s_bar(t), j & 1, wctx, kSiteSFull);
       if (!ok) break;
+      if (r == 0) FA_TRACE_EV(j, 0 + 4 * t);
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
@@ -152,6 +171,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      if (r == 0) FA_TRACE_EV(j, 1 + 4 * t);
 
       const int kv0 = j * 128;
       const bool need_mask = (kv0 + 128 > p.N) || (CAUSAL && kv0 + 127 > q0[t]);
@@ -161,15 +181,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
+      // row maximum: four independent chains of 3-input max
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 4; c < 124; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
       }
-      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+      mx0 = fmax3(mx0, s[124], s[125]);
+      mx1 = fmax3(mx1, s[126], s[127]);
+      const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c2;
       if (j == 0) {
         m_ref = m_blk;
       } else {
@@ -194,23 +217,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
           rescales += (lane == 0);
         }
       }
+      if (r == 0) FA_TRACE_EV(j, 2 + 4 * t);
       const float neg_m = -m_ref;
+      // p = 2^(s c - m): scale-shift two columns per packed FMA; row sum in
+      // two packed accumulators
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          float e[4];
+          float x[4], e[4];
+          ffma2(x[0], x[1], s[64 * half + c], s[64 * half + c + 1], c2, c2, neg_m, neg_m);
+          ffma2(x[2], x[3], s[64 * half + c + 2], s[64 * half + c + 3], c2, c2, neg_m, neg_m);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float x = fmaf(s[64 * half + c + u], c2, neg_m);
-            e[u] = ((c + u) % 16 < POLY16) ? exp2_poly(x) : ex2_mufu(x);
-          }
-          l0 += e[0];
-          l1 += e[1];
-          l2 += e[2];
-          l3 += e[3];
+          for (int u = 0; u < 4; ++u) e[u] = ((c + u) % 16 < POLY16) ? exp2_poly(x[u]) : ex2_mufu(x[u]);
+          fadd2(l0, l1, l0, l1, e[0], e[1]);
+          fadd2(l2, l3, l2, l3, e[2], e[3]);
           pk[c >> 1] = pack_bf16x2(e[0], e[1]);
           pk[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
         }
@@ -220,6 +243,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_bar(t));
+      if (r == 0) FA_TRACE_EV(j, 3 + 4 * t);
     }
 
     // ----------------------------------------------------- epilogue
@@ -269,19 +293,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       const uint32_t ring = sbase + C::kOffRing;
       auto slot_of = [&](int fill) { return fill % C::kStages; };
       auto par_of = [&](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
-      auto issue_s = [&](int t, uint32_t k_smem) {
+      // Descriptors are built once; a K step only moves the start-address
+      // field (bits 0-13, address >> 4), which never carries out for
+      // addresses inside the 228 KB shared-memory window.
+      uint64_t q_desc[QT];
+#pragma unroll
+      for (int t = 0; t < QT; ++t) q_desc[t] = make_sdesc_sw128(q_smem + t * C::kTileBytes, 0, 1024);
+      const uint64_t ring_desc_k = make_sdesc_sw128(ring, 0, 1024);
+      const uint64_t ring_desc_v = make_sdesc_sw128(ring, 16384, 1024);
+      auto issue_s = [&](int t, int slot) {
+        const uint64_t kd = ring_desc_k + (uint64_t)((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + 128u * t, make_sdesc_sw128(q_smem + t * C::kTileBytes + off, 0, 1024),
-                 make_sdesc_sw128(k_smem + off, 0, 1024), idesc_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + 128u * t, q_desc[t] + off, kd + off, idesc_s, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, uint32_t v_smem, bool acc) {
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint64_t vd = ring_desc_v + (uint64_t)((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kOCol + (uint32_t)(D * t), tmem + 128u * t + 8u * kk,
-                 make_sdesc_sw128(v_smem + kk * 2048, 16384, 1024), idesc_pv, (acc || kk > 0));
+          mma_ts(tmem + C::kOCol + (uint32_t)(D * t), tmem + 128u * t + 8u * kk, vd + (uint64_t)(kk * 128), idesc_pv,
+                 (acc || kk > 0));
       };
       bool ok = nb_max > 0;
       if (ok) ok = mbar_wait(q_bar, 0, wctx, kSiteQ);
@@ -290,7 +323,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
         tc_fence_after();
         for (int t = 0; t < QT; ++t)
           if (nb[t] > 0) {
-            issue_s(t, ring + slot_of(0) * C::kTileBytes);
+            issue_s(t, slot_of(0));
             tc_commit(s_bar(t));
           }
         tc_commit(empty_bar(slot_of(0)));
@@ -305,8 +338,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
           if (j >= nb[t]) continue;
           ok = mbar_wait(p_bar(t), j & 1, wctx, kSitePFull);
           if (!ok) break;
+          FA_TRACE_EV(j, 8 + 2 * t);
           tc_fence_after();
-          issue_pv(t, ring + slot_of(fv) * C::kTileBytes, j > 0);
+          issue_pv(t, slot_of(fv), j > 0);
           if (j + 1 < nb[t]) {
             if (!k_next) {
               ok = mbar_wait(full_bar(slot_of(fk)), par_of(fk), wctx, kSiteKFull);
@@ -314,8 +348,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
               tc_fence_after();
               k_next = true;
             }
-            issue_s(t, ring + slot_of(fk) * C::kTileBytes);
+            issue_s(t, slot_of(fk));
             tc_commit(s_bar(t));
+            FA_TRACE_EV(j, 9 + 2 * t);
           } else {
             tc_commit(o_bar(t));
           }
@@ -401,3 +436,9 @@ int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream) {
 }
 
 }  // namespace fa
+
+#ifdef FA_TRACE
+extern "C" int fa_debug_trace_fwd(unsigned long long *host_out) {
+  return cudaMemcpyFromSymbol(host_out, fa::g_trace_fwd, sizeof(fa::g_trace_fwd)) == cudaSuccess ? 0 : -5;
+}
+#endif
