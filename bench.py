@@ -232,28 +232,28 @@ def run_ours(args):
             raise fa.FaError(st, what)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    fwd_ev, main_ev = [], []
+    fwd_ev, dkdv_ev, dq_ev = [], [], []
+
+    def timed(events, record, fn):
+        if not record:
+            return fn()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        r = fn()
+        e1.record(stream)
+        events.append((e0, e1))
+        return r
 
     def step(record=False):
-        e0, e1 = (ev(), ev()) if record else (None, None)
-        if record:
-            e0.record(stream)
-        check(fa.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, sptr), "fa_fwd")
-        if record:
-            e1.record(stream)
-            fwd_ev.append((e0, e1))
+        check(timed(fwd_ev, record, lambda: fa.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, sptr)),
+              "fa_fwd")
         if not w.backward:
             return
         check(fa.fa_bwd_prepare(o, lse, dO, B, H, Hkv, N, d, ws, ws_bytes, sptr), "fa_bwd_prepare")
-        m0, m1 = (ev(), ev()) if record else (None, None)
-        if record:
-            m0.record(stream)
-        check(fa.fa_bwd_main(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, ws, ws_bytes, sptr),
-              "fa_bwd_main")
-        if record:
-            m1.record(stream)
-            main_ev.append((m0, m1))
-        check(fa.fa_bwd_finish(dq, B, H, Hkv, N, d, scale, ws, ws_bytes, sptr), "fa_bwd_finish")
+        check(timed(dkdv_ev, record, lambda: fa.fa_bwd_dkdv(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, ws,
+                                                            ws_bytes, sptr)), "fa_bwd_dkdv")
+        check(timed(dq_ev, record, lambda: fa.fa_bwd_dq(q, k, v, dO, dq, B, H, Hkv, N, d, scale, causal, ws,
+                                                        ws_bytes, sptr)), "fa_bwd_dq")
 
     launches_per_step = 4 if w.backward else 1
     for _ in range(args.warmup):
@@ -301,17 +301,25 @@ def run_ours(args):
            "config": config_of(w), "frac_of_2250_tflops": value / world / NOMINAL_BF16_TFLOPS,
            "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms}
     if w.backward:
-        main_ms = statistics.mean(a.elapsed_time(b) for a, b in main_ev)
-        src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
+        dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev)
+        dq_ms = statistics.mean(a.elapsed_time(b) for a, b in dq_ev)
         out["bwd_ms"] = ms_step - fwd_ms
         out["bwd_tflops"] = bwd_f / ((ms_step - fwd_ms) * 1e-3) / 1e12
-        achieved = bwd_f / (main_ms * 1e-3) / 1e12
+        out["dkdv_ms"], out["dq_ms"] = dkdv_ms, dq_ms
+        # executed GEMM flops of each backward kernel: dK/dV recomputes S^T and dP^T
+        # (4 GEMMs of 2 N^2 d per head), dQ recomputes S and dP (3 GEMMs)
+        gemm = fwd_f / 2  # one N x N x d GEMM pass over all heads, causal halving included
+        kern = ("bwd_dkdv_kernel", dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
+            ("bwd_dq_kernel", dq_ms, 3 * gemm, "fa_bwd.cu")
+        name, kms, kflops, _ = kern
+        src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "fa_internal.h"])
+        achieved = kflops / (kms * 1e-3) / 1e12
         out["roofline"] = {
-            "bound": "tensor", "kernel": "bwd_main_kernel", "achieved": achieved,
+            "bound": "tensor", "kernel": name, "achieved": achieved,
             "peak": peaks["sustained"], "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
             "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
-            "flops_per_launch": bwd_f, "launch_ms": main_ms,
-            "traffic": profiled_traffic(f"bwd_main_{args.workload}.md", src),
+            "flops_per_launch": kflops, "launch_ms": kms,
+            "traffic": profiled_traffic(f"{name}_{args.workload}.md", src),
         }
     else:
         src = kernel_source_hash(["fa_fwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
@@ -321,7 +329,7 @@ def run_ours(args):
             "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
             "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
             "flops_per_launch": fwd_f, "launch_ms": fwd_ms,
-            "traffic": profiled_traffic(f"fwd_{args.workload}.md", src),
+            "traffic": profiled_traffic(f"fa_fwd_kernel_{args.workload}.md", src),
         }
     out["gpu_launches"] = launches_per_step * args.steps
     out["clocks"] = clocks

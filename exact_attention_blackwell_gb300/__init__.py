@@ -31,8 +31,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_prepare": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
-    "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
-    "fa_bwd_finish": (_I, [_P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_exp2_poly": (_I, [_P, _P, _LL, _P]),
     "fa_last_device_status": (_I, [_P]),
@@ -107,16 +107,16 @@ def fa_bwd_prepare(o, lse, dO, B, H, Hkv, N, d, workspace, workspace_bytes, stre
                                 int(workspace_bytes), _stream(stream))
 
 
-def fa_bwd_main(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes,
+def fa_bwd_dkdv(q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes,
                 stream=None) -> int:
-    return lib().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
+    return lib().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
                              float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
                              _stream(stream))
 
 
-def fa_bwd_finish(dq, B, H, Hkv, N, d, scale, workspace, workspace_bytes, stream=None) -> int:
-    return lib().fa_bwd_finish(_ptr(dq), B, H, Hkv, N, d, float(scale), _ptr(workspace), int(workspace_bytes),
-                               _stream(stream))
+def fa_bwd_dq(q, k, v, dO, dq, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), B, H, Hkv, N, d, float(scale),
+                           int(bool(causal)), _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, stream=None) -> int:

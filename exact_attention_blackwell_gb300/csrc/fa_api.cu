@@ -86,31 +86,8 @@ int get_encoder() {
 }
 }  // namespace
 
-int encode_f32_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows) {
-  if (get_encoder() != FA_OK) return FA_ERR_CUDA;
-  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hx, (cuuint64_t)N, (cuuint64_t)B};
-  const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)Hx * d * 4, (cuuint64_t)N * Hx * d * 4};
-  const cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
-}
-
 int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_encode == nullptr) {
-      void *fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return FA_ERR_CUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  if (get_encoder() != FA_OK) return FA_ERR_CUDA;
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hx, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hx * d * 2, (cuuint64_t)N * Hx * d * 2};
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
@@ -163,10 +140,9 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {
   if (check_common(B, H, Hkv, N, d, 1.0f) != FA_OK) return 0;
   const size_t Npad = ((size_t)N + 127) / 128 * 128;
-  const size_t acc = (size_t)B * N * H * d * sizeof(float);
   const size_t rows = (size_t)B * H * Npad * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return up(acc) + 2 * up(rows);
+  return 2 * up(rows);
 }
 
 }  // extern "C"
@@ -175,34 +151,33 @@ namespace {
 
 // Validation and parameter set-up shared by fa_bwd and its three stages.
 // Pointers passed as nullptr are not needed by the stage and are not checked.
-int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const void *dO, const void *dk,
-              const void *dv, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
-              size_t workspace_bytes, bool maps) {
+int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const void *dO, const void *dq,
+              const void *dk, const void *dv, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
+              size_t workspace_bytes) {
   int rc = check_common(B, H, Hkv, N, d, scale);
   if (rc != FA_OK) return rc;
   if (d == 256) return FA_ERR_UNSUPPORTED;
-  for (const void *x : {q, k, v, dO, dk, dv})
+  for (const void *x : {q, k, v, dO, dq, dk, dv})
     if (x && !aligned16(x)) return FA_ERR_ALIGNMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FA_ERR_WORKSPACE;
   if ((rc = check_device()) != FA_OK) return rc;
   std::memset(p, 0, sizeof(*p));
-  if (maps && (encode_bf16_tile_map(&p->tm_q, q, B, N, H, d, 128) ||
-               encode_bf16_tile_map(&p->tm_k, k, B, N, Hkv, d, 128) ||
-               encode_bf16_tile_map(&p->tm_v, v, B, N, Hkv, d, 128) ||
-               encode_bf16_tile_map(&p->tm_do, dO, B, N, H, d, 128) ||
-               encode_bf16_tile_map(&p->tm_dk, dk, B, N, Hkv, d, 128) ||
-               encode_bf16_tile_map(&p->tm_dv, dv, B, N, Hkv, d, 128)))
+  // tensor maps of the tensors this stage touches (nullptr: not used by it)
+  if ((q && encode_bf16_tile_map(&p->tm_q, q, B, N, H, d, 128)) ||
+      (k && encode_bf16_tile_map(&p->tm_k, k, B, N, Hkv, d, 128)) ||
+      (v && encode_bf16_tile_map(&p->tm_v, v, B, N, Hkv, d, 128)) ||
+      (dO && encode_bf16_tile_map(&p->tm_do, dO, B, N, H, d, 128)) ||
+      (dq && encode_bf16_tile_map(&p->tm_dq, dq, B, N, H, d, 128)) ||
+      (dk && encode_bf16_tile_map(&p->tm_dk, dk, B, N, Hkv, d, 128)) ||
+      (dv && encode_bf16_tile_map(&p->tm_dv, dv, B, N, Hkv, d, 128)))
     return FA_ERR_CUDA;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t Npad = ((size_t)N + 127) / 128 * 128;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  p->dq_acc = reinterpret_cast<float *>(ws);
-  if (maps && encode_f32_tile_map(&p->tm_dqacc, p->dq_acc, B, N, H, d, 128)) return FA_ERR_CUDA;
-  p->lse2 = reinterpret_cast<float *>(ws + up((size_t)B * N * H * d * sizeof(float)));
-  p->delta = reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(p->lse2) +
-                                             up((size_t)B * H * Npad * sizeof(float)));
+  p->lse2 = reinterpret_cast<float *>(ws);
+  p->delta = reinterpret_cast<const float *>(ws + up((size_t)B * H * Npad * sizeof(float)));
   p->status = device_status_ptr();
   if (!p->status) return FA_ERR_CUDA;
   p->B = B;
@@ -225,30 +200,29 @@ int fa_bwd_prepare(const void *o, const float *lse, const void *dO, int B, int H
   if (!o || !lse || !dO) return FA_ERR_INVALID_ARG;
   if (!aligned16(o) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
   BwdParams p;
-  int rc = setup_bwd(&p, nullptr, nullptr, nullptr, dO, nullptr, nullptr, B, H, Hkv, N, d, 1.0f, workspace,
-                     workspace_bytes, false);
+  int rc = setup_bwd(&p, nullptr, nullptr, nullptr, dO, nullptr, nullptr, nullptr, B, H, Hkv, N, d, 1.0f, workspace,
+                     workspace_bytes);
   if (rc != FA_OK) return rc;
   return launch_bwd_pre(p, d, o, dO, lse, static_cast<cudaStream_t>(stream));
 }
 
-int fa_bwd_main(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv, int B, int H,
+int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv, int B, int H,
                 int Hkv, int N, int d, float scale, int causal, void *workspace, size_t workspace_bytes,
                 void *stream) {
   if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
   BwdParams p;
-  int rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes, true);
+  int rc = setup_bwd(&p, q, k, v, dO, nullptr, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes);
   if (rc != FA_OK) return rc;
-  return launch_bwd_main(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+  return launch_bwd_dkdv(p, d, causal != 0, static_cast<cudaStream_t>(stream));
 }
 
-int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
-                  size_t workspace_bytes, void *stream) {
-  if (!dq) return FA_ERR_INVALID_ARG;
+int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dO, void *dq, int B, int H, int Hkv, int N,
+              int d, float scale, int causal, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !dO || !dq) return FA_ERR_INVALID_ARG;
   BwdParams p;
-  int rc = setup_bwd(&p, nullptr, nullptr, nullptr, nullptr, dq, nullptr, B, H, Hkv, N, d, scale, workspace,
-                     workspace_bytes, false);
+  int rc = setup_bwd(&p, q, k, v, dO, dq, nullptr, nullptr, B, H, Hkv, N, d, scale, workspace, workspace_bytes);
   if (rc != FA_OK) return rc;
-  return launch_bwd_post(p, d, dq, static_cast<cudaStream_t>(stream));
+  return launch_bwd_dq(p, d, causal != 0, static_cast<cudaStream_t>(stream));
 }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
@@ -257,14 +231,14 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int rc = check_common(B, H, Hkv, N, d, scale);
   if (rc != FA_OK) return rc;
-  if (!aligned16(o) || !aligned16(dq) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
+  if (!aligned16(o) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
   BwdParams p;
-  if ((rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes, true)) != FA_OK)
+  if ((rc = setup_bwd(&p, q, k, v, dO, dq, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes)) != FA_OK)
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
-  if ((rc = launch_bwd_main(p, d, causal != 0, s)) != FA_OK) return rc;
-  return launch_bwd_post(p, d, dq, s);
+  if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_dq(p, d, causal != 0, s);
 }
 
 }  // extern "C"
@@ -274,9 +248,9 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 // plug-ins living inside a host framework that owns every device allocation
 // through its own pool, and serving or training loops that forbid cudaMalloc
 // after start-up because it synchronises the device and fragments memory.
-// fa_bwd_noalloc serves them: its scratch (the fp32 dQ accumulator and the
-// per-row D / log2-LSE terms that fa_bwd keeps in the caller's workspace) is
-// this file-scope device array instead.  Every GPU that loads the library holds
+// fa_bwd_noalloc serves them: its scratch (the per-row D and log2-LSE terms
+// that fa_bwd keeps in the caller's workspace) is this file-scope device array
+// instead.  Every GPU that loads the library holds
 // it until the process exits.
 namespace fa {
 namespace {
@@ -318,15 +292,15 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
   void *ws = nullptr;
   if ((rc = scratch_address(&ws)) != FA_OK) return rc;
   BwdParams p;
-  if ((rc = setup_bwd(&p, q, k, v, dO, dk, dv, B, H, Hkv, N, d, scale, ws, kNoAllocScratchBytes, true)) != FA_OK)
+  if ((rc = setup_bwd(&p, q, k, v, dO, dq, dk, dv, B, H, Hkv, N, d, scale, ws, kNoAllocScratchBytes)) != FA_OK)
     return rc;
   // bwd_pre writes every part of the scratch that the other launches read
-  // (zeroes the accumulator, fills D and log2-LSE), so stale contents left by
-  // an earlier call do not matter.
+  // (D and log2-LSE of every padded row), so stale contents left by an earlier
+  // call do not matter.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
-  if ((rc = launch_bwd_main(p, d, causal != 0, s)) != FA_OK) return rc;
-  return launch_bwd_post(p, d, dq, s);
+  if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_dq(p, d, causal != 0, s);
 }
 
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {

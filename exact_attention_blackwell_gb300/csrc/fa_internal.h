@@ -37,10 +37,9 @@ struct FwdParams {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
   CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
-  CUtensorMap tm_dqacc;                 // reduce-add into the fp32 accumulator [B, N, H, d], box 32 x 128
-  float *lse2;                          // [B, H, Npad] LSE * log2(e)
-  const float *delta;                   // [B, H, Npad] D = rowsum(dO * O)
-  float *dq_acc;                        // [B, N, H, d] fp32 accumulator
+  CUtensorMap tm_dq;                    // store [B, N, H, d]
+  float *lse2;                          // [B, H, Npad] LSE * log2(e) (workspace)
+  const float *delta;                   // [B, H, Npad] D = rowsum(dO * O) (workspace)
   unsigned *status;
   int B, H, Hkv, N;
   float scale;       // softmax scale
@@ -53,13 +52,11 @@ unsigned *device_status_ptr();
 // Encodes a 4-D tensor map over a bf16 [B, N, Hx, d] tensor, box = 64 columns x
 // `box_rows` rows of one head, 128-byte swizzle.  Returns 0 on success.
 int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows);
-// Same for an fp32 [B, N, Hx, d] tensor, box = 32 columns x `box_rows` rows.
-int encode_f32_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows);
 
 int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream);
 // The three launches of the backward pass (fa_bwd runs them in this order).
 int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, const float *lse, cudaStream_t stream);
-int launch_bwd_main(const BwdParams &p, int d, bool causal, cudaStream_t stream);
-int launch_bwd_post(const BwdParams &p, int d, void *dq, cudaStream_t stream);
+int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream);
+int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream);
 
 }  // namespace fa

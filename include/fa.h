@@ -64,39 +64,41 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
 
-/* Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
- * accumulator [B,N,H,d] plus two fp32 row-term arrays [B,H,Npad] (D and the
- * log2-scaled LSE), Npad = N rounded up to a multiple of 128; each part
- * starts on a 256-byte boundary.
+/* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row-term
+ * arrays [B,H,Npad] (D = rowsum(dO * O) and the log2-scaled LSE), Npad = N
+ * rounded up to a multiple of 128, each starting on a 256-byte boundary.
  * Returns 0 for sizes fa_bwd would reject. */
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse from the forward, and dO [B,N,H,d].
  * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  Head dims 64 and 128
- * (d = 256 returns FA_ERR_UNSUPPORTED).  `workspace` is caller
- * owned device memory of at least fa_bwd_workspace_bytes() bytes, 256-byte
- * aligned; its contents on entry do not matter and are overwritten.  The call
- * is not deterministic in the last bits (dQ is summed with atomics). */
+ * (d = 256 returns FA_ERR_UNSUPPORTED).  `workspace` is caller owned device
+ * memory of at least fa_bwd_workspace_bytes() bytes, 256-byte aligned; its
+ * contents on entry do not matter and are overwritten.  No atomics: results
+ * are bitwise reproducible for the same inputs. */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dO, void *dq, void *dk, void *dv,
            int B, int H, int Hkv, int N, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
 
 /* The three launches fa_bwd makes, for callers that schedule them separately
- * (same arguments and rules as fa_bwd; run them in this order on one stream,
- * with the same workspace):
+ * (same arguments and rules as fa_bwd; run fa_bwd_prepare first, then the
+ * other two in either order, on one stream or ordered streams, with the same
+ * workspace):
  *   fa_bwd_prepare: D = rowsum(dO * O) and the log2-scaled LSE into the
- *                   workspace, the dQ accumulator zeroed (memory bound);
- *   fa_bwd_main:    the fused kernel: recomputes P from LSE, writes dk and dv,
- *                   accumulates dQ in the workspace;
- *   fa_bwd_finish:  dq = bf16(scale * accumulator). */
+ *                   workspace (memory bound);
+ *   fa_bwd_dkdv:    the key/value-stationary kernel: recomputes P from LSE,
+ *                   writes dk and dv;
+ *   fa_bwd_dq:      the query-stationary kernel: recomputes S, P and dP,
+ *                   writes dq. */
 int fa_bwd_prepare(const void *o, const float *lse, const void *dO, int B, int H, int Hkv, int N, int d,
                    void *workspace, size_t workspace_bytes, void *stream);
-int fa_bwd_main(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv,
+int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dO, void *dk, void *dv,
                 int B, int H, int Hkv, int N, int d, float scale, int causal,
                 void *workspace, size_t workspace_bytes, void *stream);
-int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale,
-                  void *workspace, size_t workspace_bytes, void *stream);
+int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dO, void *dq,
+              int B, int H, int Hkv, int N, int d, float scale, int causal,
+              void *workspace, size_t workspace_bytes, void *stream);
 
 /* Backward pass that allocates nothing and takes no workspace.  The pages have
  * no counterpart: this entry point exists for callers that cannot allocate
@@ -104,7 +106,7 @@ int fa_bwd_finish(void *dq, int B, int H, int Hkv, int N, int d, float scale,
  * framework that owns all device memory through its own pool; a serving or
  * training loop that forbids cudaMalloc after start-up, since it synchronises
  * the device and fragments memory).  Same arguments, results and rules as
- * fa_bwd, except that the scratch fa_bwd keeps in the caller's workspace lives
+ * fa_bwd, except that the row terms fa_bwd keeps in the caller's workspace live
  * in one static device array of FA_BWD_NOALLOC_SCRATCH_BYTES bytes inside the
  * library, which every GPU that loads the library holds until the process
  * exits.

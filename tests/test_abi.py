@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_prepare", "fa_bwd_main", "fa_bwd_finish",
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_prepare", "fa_bwd_dkdv", "fa_bwd_dq",
               "fa_exp2_poly", "fa_last_device_status", "fa_status_string"):
         assert n in names
 
@@ -95,19 +95,20 @@ def test_bwd_stages_reject_bad_arguments(lib):
     assert fa.fa_bwd_prepare(None, A, A, 1, 2, 2, 256, 128, A, nb, 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd_prepare(A, A + 2, A, 1, 2, 2, 256, 128, A, nb, 0) == fa.FA_ERR_ALIGNMENT
     assert fa.fa_bwd_prepare(A, A, A, 1, 2, 2, 256, 128, A, nb - 4, 0) == fa.FA_ERR_WORKSPACE
-    assert fa.fa_bwd_main(A, A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_main(A, A, A, A, A, A, 1, 2, 2, 256, 256, 0.1, 0, A, nb, 0) == fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_bwd_main(A, A, A, A, A + 8, A, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_ALIGNMENT
-    assert fa.fa_bwd_finish(None, 1, 2, 2, 256, 128, 0.1, A, nb, 0) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_finish(A, 1, 2, 2, 256, 128, -0.1, A, nb, 0) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_finish(A, 1, 2, 2, 256, 128, 0.1, None, nb, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd_dkdv(A, A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_dkdv(A, A, A, A, A, A, 1, 2, 2, 256, 256, 0.1, 0, A, nb, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_dkdv(A, A, A, A, A + 8, A, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_ALIGNMENT
+    assert fa.fa_bwd_dq(A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_dq(A, A, A, A, A, 1, 2, 2, 256, 128, -0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_dq(A, A, A, A, A, 1, 2, 2, 256, 128, 0.1, 0, None, nb, 0) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd_dq(A, A, A, A + 4, A, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_ALIGNMENT
 
 
 def test_workspace_size():
     B, H, Hkv, N, d = 2, 4, 2, 1000, 128
     up = lambda x: (x + 255) // 256 * 256
     Npad = (N + 127) // 128 * 128
-    assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d) == up(B * N * H * d * 4) + 2 * up(B * H * Npad * 4)
+    assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d) == 2 * up(B * H * Npad * 4)
     assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, 96) == 0
     assert fa.fa_bwd_workspace_bytes(0, H, Hkv, N, d) == 0
 

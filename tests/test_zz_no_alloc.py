@@ -53,7 +53,7 @@ def test_matches_workspace_backward_on_two_calls_in_a_row():
 
 
 def test_rejects_sizes_beyond_the_builtin_scratch():
-    B, H, Hkv, N, d = 1, 16, 16, 8192, 128
+    B, H, Hkv, N, d = 64, 64, 64, 8192, 128
     assert fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d) > fa.FA_BWD_NOALLOC_SCRATCH_BYTES
     a = 0x10000  # never dereferenced: the size check comes before any launch
     st = fa.fa_bwd_noalloc(a, a, a, a, a, a, a, a, a, B, H, Hkv, N, d, 0.088, 0)
