@@ -149,7 +149,11 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
 template <int D>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128-row bf16 tile
-  static constexpr int kStages = 2;          // (Q_i, dO_i, LSE2_i, D_i) ring depth
+  // Q_i and dO_i stream through a ring of single-tile slots (Q_i = fill 2i,
+  // dO_i = fill 2i + 1), so loads run more than two iterations ahead; the
+  // per-iteration LSE2 / D rows go through their own small ring.
+  static constexpr int kSlots = (D == 64) ? 10 : 5;
+  static constexpr int kRowStages = 2;  // own full/empty barriers, released after each dS
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8, kLoadWarp = 9;
   static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -157,12 +161,12 @@ struct DkdvCfg {
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffStage = 2 * kTile;  // stage s: Q at +2s*kTile, dO at +(2s+1)*kTile
-  static constexpr int kOffDS = kOffStage + 2 * kStages * kTile;  // dS^T, 128 x 128 bf16
-  static constexpr int kOffRows = kOffDS + 128 * 128 * 2;          // stage s: LSE2 at +1024s, D at +1024s+512
-  enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarS = kBarEmpty0 + kStages, kBarDP, kBarP, kBarDS,
-         kBarDSFree, kBarFinal, kBarDrain, kNumBars };
-  static constexpr int kOffBar = kOffRows + 1024 * kStages;
+  static constexpr int kOffRing = 2 * kTile;
+  static constexpr int kOffRows = kOffRing + kSlots * kTile;  // row stage r: LSE2 at +1024r, D at +1024r+512
+  enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
+         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages, kBarDP, kBarP, kBarDS,
+         kBarFinal, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked in the kernel)
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -193,7 +197,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   const int kv0 = jt * 128;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), (i == C::kBarP || i == C::kBarDS) ? 256u : 1u);
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
+      mbar_init(bar(i), all ? 256u : 1u);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -214,50 +221,57 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
 
   if (warp < 8) {
     // ===================================================== P^T and dS^T, one warpgroup per 64 query columns
+    // P stays in registers (fp32) from its computation to dS; P^T (bf16) goes
+    // to TMEM over the S^T columns for the dV MMA, dS^T (bf16) over the dP^T
+    // columns once they have been read, for the dK MMA.
     const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
     const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;  // S^T columns of this warpgroup
     const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first 32
     const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
+    const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
     const bool row_valid = kv0 + r < p.N;
-    uint8_t *ds_tile = smem + C::kOffDS;
     bool ok = true;
     for (int it = 0; it < n_iter && ok; ++it) {
-      const int st = it % C::kStages;
+      const int rs = it % C::kRowStages;
       const int i = i_start + it % per_head;
-      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * st) + 64 * wg;
+      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
       const float *dlt_s = lse2_s + 128;
       // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
       ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
+      if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
       if (!ok) break;
       if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
       tc_fence_after();
-      const bool diag = CAUSAL && (i == jt);
+      const bool need_mask = !row_valid || (CAUSAL && i == jt);  // key rows past N, or the diagonal tile
       uint32_t sv[2][32];
       tmem_ld_32x32b_x32(s_tm, sv[0]);
       tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
       tmem_wait_ld(sv[0]);
       reg_tie(sv[1]);
+      float pe[64];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
-          float x[4], pe[4];
+          float x[4];
           ffma2(x[0], x[1], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]), p.scale_log2, p.scale_log2,
                 -l4.x, -l4.y);
           ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), p.scale_log2,
                 p.scale_log2, -l4.z, -l4.w);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) pe[u] = ex2_mufu(x[u]);
-          const int qc = 64 * wg + 32 * c + k;  // query column within tile i
+          for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
+          if (need_mask) {
+            const int qc = 64 * wg + 32 * c + k;  // query column within tile i
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (!row_valid || (diag && qc + u < r)) pe[u] = 0.f;
-          w[k >> 1] = pack_bf16x2(pe[0], pe[1]);
-          w[(k >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+            for (int u = 0; u < 4; ++u)
+              if (!row_valid || qc + u < r) pe[32 * c + k + u] = 0.f;
+          }
+          w[k >> 1] = pack_bf16x2(pe[32 * c + k], pe[32 * c + k + 1]);
+          w[(k >> 1) + 1] = pack_bf16x2(pe[32 * c + k + 2], pe[32 * c + k + 3]);
         }
         tmem_st_32x32b_x16(p_tm + 16 * c, w);
       }
@@ -265,46 +279,43 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(bar(C::kBarP));
       if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
-      // ---- dS^T = P^T (dP^T - D) -> shared memory (bf16, 128B swizzle, box = wg)
+      // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
       ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
-      if (ok && it > 0) ok = mbar_wait_warp(bar(C::kBarDSFree), (it - 1) & 1, wctx, kBSiteDSFree);
       if (!ok) break;
       if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
       tc_fence_after();
-      uint32_t dpv[2][32], pv[32];
+      uint32_t dpv[2][32];
       tmem_ld_32x32b_x32(dp_tm, dpv[0]);
       tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
-      tmem_ld_32x32b_x32(p_tm, pv);
       tmem_wait_ld(dpv[0]);
       reg_tie(dpv[1]);
-      reg_tie(pv);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
           const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + 32 * c + k);
-          const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[16 * c + (k >> 1)]);
-          const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162 *>(&pv[16 * c + (k >> 1) + 1]);
           float t[4], ds[4];
           fadd2(t[0], t[1], __uint_as_float(dpv[c][k]), __uint_as_float(dpv[c][k + 1]), -d4.x, -d4.y);
           fadd2(t[2], t[3], __uint_as_float(dpv[c][k + 2]), __uint_as_float(dpv[c][k + 3]), -d4.z, -d4.w);
-          fmul2(ds[0], ds[1], __low2float(p01), __high2float(p01), t[0], t[1]);
-          fmul2(ds[2], ds[3], __low2float(p23), __high2float(p23), t[2], t[3]);
+          fmul2(ds[0], ds[1], pe[32 * c + k], pe[32 * c + k + 1], t[0], t[1]);
+          fmul2(ds[2], ds[3], pe[32 * c + k + 2], pe[32 * c + k + 3], t[2], t[3]);
           w[k >> 1] = pack_bf16x2(ds[0], ds[1]);
           w[(k >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        st_swizzled_32cols(ds_tile, r, 64 * wg + 32 * c, w);
+        tmem_st_32x32b_x16(ds_tm + 16 * c, w);
       }
-      fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarDS));
+      mbar_arrive(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
       if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
     }
-    // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via stage 0's Q / dO slots)
+    // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
+    //      drained once every MMA has completed)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
-    uint8_t *stage = smem + C::kOffStage + wg * C::kTile;
+    uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
     if (ok) acc_to_smem<D>(tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK), stage, r, 0, wg == 0 ? 1.0f : p.scale);
     fence_proxy_async_smem();
     if (wg == 0) named_bar_sync(1, 128);
@@ -317,72 +328,87 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
-    // Order: S_0 dP_0 | dV_0 [dS_0] S_1 dK_0 dP_1 | dV_1 [dS_1] S_2 dK_1 dP_2 | ...
-    // S_{i+1} and dP_{i+1} overwrite the S/P and dP columns only after dS_i has
-    // been formed (it reads both); the tensor pipe runs one thread's MMAs in
-    // order, so dV_i has read P^T_i before S_{i+1} writes there.
+    // Order: S_0 dP_0 | [P_0] dV_0 S_1 [dS_0] dK_0 dP_1 | [P_1] dV_1 S_2 [dS_1] dK_1 dP_2 | ...
+    // P^T_i (S^T columns) is read by dV_i, which precedes S_{i+1}; dS^T_i (dP^T
+    // columns) is read by dK_i, which precedes dP_{i+1}: the tensor pipe runs
+    // one thread's MMAs in order.  The elementwise warps have loaded S^T_i and
+    // dP^T_i into registers before they signal P_i and dS_i.
     if (lane == 0) {
       constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_dv = make_idesc_bf16(128, D, false, true);     // dV (A in TMEM), dK
+      constexpr uint32_t id_dv = make_idesc_bf16(128, D, false, true);     // dV, dK (A in TMEM, B MN-major)
       const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
       const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
-      const uint64_t ds_d = make_sdesc_sw128(sbase + C::kOffDS, 0, 1024);
-      const uint64_t st_d = make_sdesc_sw128(sbase + C::kOffStage, 0, 1024);        // K-major view
-      const uint64_t st_dmn = make_sdesc_sw128(sbase + C::kOffStage, 16384, 1024);  // MN-major view
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);        // K-major view
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);   // MN-major view
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
-      auto issue_s = [&](int it) {  // S^T = K Q^T
-        const uint64_t q_off = (uint64_t)((2 * (it % C::kStages) * C::kTile) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColS, k_d + kmaj(kk), st_d + q_off + kmaj(kk), id_kk, kk > 0);
-        tc_commit(bar(C::kBarS));
+      auto slot_of = [](int fill) { return fill % C::kSlots; };
+      auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kTile) >> 4); };
+      auto full_ok = [&](int fill) {
+        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
       };
-      auto issue_dp = [&](int it) {  // dP^T = V dO^T
-        const uint64_t do_off = (uint64_t)(((2 * (it % C::kStages) + 1) * C::kTile) >> 4);
+      auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, v_d + kmaj(kk), st_d + do_off + kmaj(kk), id_kk, kk > 0);
+          mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
+        tc_commit(bar(C::kBarS));
+      };
+      auto issue_dp = [&](int it) {  // dP^T = V dO^T   (dO_it is fill 2 it + 1)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj(kk), id_kk, kk > 0);
         tc_commit(bar(C::kBarDP));
       };
+      // A operand in TMEM: the query columns 64w.. of warpgroup w start at
+      // column 64w of the region; 16 query rows per K step = 8 columns.
+      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
       bool ok = mbar_wait(bar(C::kBarKV), 0, wctx, kBSiteKV);
-      if (ok) ok = mbar_wait(bar(C::kBarFull0), 0, wctx, kBSiteFull);
+      if (ok) ok = full_ok(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
+        ok = full_ok(1);
+      }
+      if (ok) {
+        tc_fence_after();
         issue_dp(0);
       }
       for (int it = 0; it < n_iter && ok; ++it) {
-        const int st = it % C::kStages;
+        const bool more = it + 1 < n_iter;
         FA_TRACE_EV(0, it, 8);
-        // dV += P^T dO   (A = P^T in TMEM: query columns 64w.. at column 64w, two bf16 per column;
-        //                 B = dO_i MN-major)
         ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
         if (!ok) break;
         FA_TRACE_EV(0, it, 9);
         tc_fence_after();
-        const uint64_t do_mn = st_dmn + (uint64_t)(((2 * st + 1) * C::kTile) >> 4);
-        const uint64_t q_mn = st_dmn + (uint64_t)((2 * st * C::kTile) >> 4);
+        // dV += P^T dO_it
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + 64u * (kk >> 2) + 8u * (kk & 3), do_mn + (uint64_t)(kk * 128),
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
                  id_dv, (it > 0 || kk > 0));
+        tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
+        if (more) {
+          FA_TRACE_EV(0, it, 12);
+          ok = full_ok(2 * it + 2);
+          if (!ok) break;
+          FA_TRACE_EV(0, it, 13);
+          tc_fence_after();
+          issue_s(it + 1);
+        }
         ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
         FA_TRACE_EV(0, it, 10);
         tc_fence_after();
-        const bool more = it + 1 < n_iter;
-        if (more) {
-          ok = mbar_wait(bar(C::kBarFull0 + (it + 1) % C::kStages), ((it + 1) / C::kStages) & 1, wctx, kBSiteFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(it + 1);
-        }
-        // dK += dS^T Q  (A = dS^T K-major [key][query]; B = Q_i MN-major)
+        // dK += dS^T Q_it
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::kColDK, ds_d + kmaj(kk), q_mn + (uint64_t)(kk * 128), id_dv, (it > 0 || kk > 0));
-        tc_commit(bar(C::kBarDSFree));
-        tc_commit(bar(C::kBarEmpty0 + st));
-        if (more) issue_dp(it + 1);
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128), id_dv,
+                 (it > 0 || kk > 0));
+        tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it)));  // Q_it consumed (S_it, dK_it)
+        if (more) {
+          ok = full_ok(2 * it + 3);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
         FA_TRACE_EV(0, it, 11);
       }
       tc_commit(bar(C::kBarFinal));
@@ -402,27 +428,40 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
         tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, kv0, b);
       }
       bool ok = true;
-      int it = 0;
-      for (; it < n_iter && ok; ++it) {
-        const int st = it % C::kStages;
+      int fill = 0, rows_issued = 0;
+      for (int it = 0; it < n_iter && ok; ++it) {
         const int hh = kh * g + it / per_head;
         const int i = i_start + it % per_head;
-        ok = mbar_wait(bar(C::kBarEmpty0 + st), ((it / C::kStages) & 1) ^ 1, wctx, kBSiteEmpty);
-        if (!ok) break;
-        const uint32_t fb = bar(C::kBarFull0 + st);
-        mbar_arrive_expect_tx(fb, 2 * C::kTile + 1024);
-        const uint32_t q_s = sbase + C::kOffStage + 2 * st * C::kTile;
-        for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_4d_hint(q_s + bx * 16384, &p.tm_q, fb, bx * 64, hh, i * 128, b, keep);
-          tma_load_4d_hint(q_s + C::kTile + bx * 16384, &p.tm_do, fb, bx * 64, hh, i * 128, b, keep);
+        for (int t = 0; t < 2 && ok; ++t, ++fill) {  // t = 0: Q_it, t = 1: dO_it
+          const int s = fill % C::kSlots;
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), ((fill / C::kSlots) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          const uint32_t fb = bar(C::kBarFull0 + s);
+          mbar_arrive_expect_tx(fb, C::kTile);
+          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, i * 128, b, keep);
         }
+        if (!ok) break;
+        // LSE2 / D rows of iteration it, into row stage it % kRowStages once the
+        // elementwise warps are done with iteration it - kRowStages
+        const int rs = it % C::kRowStages;
+        ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
+        if (!ok) break;
+        const uint32_t rb = bar(C::kBarRowFull0 + rs);
+        mbar_arrive_expect_tx(rb, 1024);
         const size_t roff = ((size_t)b * p.H + hh) * Npad + (size_t)i * 128;
-        bulk_load(sbase + C::kOffRows + 1024 * st, p.lse2 + roff, 512, fb);
-        bulk_load(sbase + C::kOffRows + 1024 * st + 512, p.delta + roff, 512, fb);
+        const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+        bulk_load(rdst, p.lse2 + roff, 512, rb);
+        bulk_load(rdst + 512, p.delta + roff, 512, rb);
+        ++rows_issued;
       }
       const uint64_t t0 = global_timer_ns();
-      for (int f = max(0, it - C::kStages); f < it; ++f)
-        while (!mbar_test(bar(C::kBarFull0 + f % C::kStages), (f / C::kStages) & 1) &&
+      for (int f = max(0, fill - C::kSlots); f < fill; ++f)
+        while (!mbar_test(bar(C::kBarFull0 + f % C::kSlots), (f / C::kSlots) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
+        while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
                global_timer_ns() - t0 < kWaitLimitNs) {}
       while (!mbar_test(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
@@ -440,26 +479,27 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
 template <int D>
 struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kStages = (D == 64) ? 6 : 4;  // K_j / V_j ring (alternating)
+  static constexpr int kStages = (D == 64) ? 14 : 7;  // K_j / V_j ring (alternating)
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8, kLoadWarp = 9;
-  static constexpr int kColS = 0;  // two S/dS buffers at 0 and 128
-  static constexpr int kColDP = 256, kColDQ = 384;
+  // TMEM: S (fp32), dP (fp32; dS bf16 over it once read), dQ (fp32), and the
+  // CTA's Q and dO tiles (bf16, two per column) as A operands of the S and dP MMAs.
+  static constexpr int kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
   static constexpr int kTmemCols = 512;
-  static_assert(kColDQ + D <= kTmemCols, "TMEM budget");
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = kTile;
-  static constexpr int kOffRing = 2 * kTile;
+  static_assert(kColDO + D / 2 <= kTmemCols, "TMEM budget");
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffStage = 0;  // dQ epilogue staging: ring slot 0, drained by then
   static constexpr int kOffBar = kOffRing + kStages * kTile;
-  enum { kBarQ, kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarS0 = kBarEmpty0 + kStages, kBarS1, kBarDP, kBarDS,
-         kBarFinal, kBarDrain, kNumBars };
+  enum { kBarQdo, kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarS = kBarEmpty0 + kStages, kBarSFree, kBarDP,
+         kBarDS, kBarFinal, kBarDrain, kNumBars };
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p, const __nv_bfloat16 *q,
+                                                        const __nv_bfloat16 *dO) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -481,7 +521,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   const int nb = CAUSAL ? it_q + 1 : n_q;  // key tiles this query tile sees
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), i == C::kBarDS ? 256u : 1u);
+    for (int i = 0; i < C::kNumBars; ++i)
+      mbar_init(bar(i), (i == C::kBarQdo || i == C::kBarSFree || i == C::kBarDS) ? 256u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -490,10 +531,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     tmem_relinquish();
   }
   if (warp == C::kLoadWarp && lane == 0) {
-    prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
-    prefetch_tmap(&p.tm_do);
     prefetch_tmap(&p.tm_dq);
   }
   tc_fence_before();
@@ -506,15 +545,45 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;
     const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
+    const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first 32 of this warpgroup's dP columns
     const int q_row = q0 + r;
+    {
+      // Q (warpgroup 0) or dO (warpgroup 1): this thread's row, bf16 pairs in
+      // memory order, into TMEM as the A operand of the S / dP MMAs.
+      const __nv_bfloat16 *src = wg == 0 ? q : dO;
+      uint32_t row[D / 2];
+      if (q_row < p.N) {
+        const uint4 *g = reinterpret_cast<const uint4 *>(src + (((size_t)b * p.N + q_row) * p.H + h) * D);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          const uint4 x = g[v];
+          row[4 * v] = x.x;
+          row[4 * v + 1] = x.y;
+          row[4 * v + 2] = x.z;
+          row[4 * v + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < D / 2; ++v) row[v] = 0u;
+      }
+      const uint32_t dst = tmem + lane_off + (wg == 0 ? C::kColQ : C::kColDO);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&row[32 * c]);
+        tmem_st_32x32b_x32(dst + 32 * c, part);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarQdo));
+    }
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
     const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
     const float dlt = p.delta[rw];
     bool ok = true;
     for (int j = 0; j < nb && ok; ++j) {
-      const uint32_t s_tm = tmem + lane_off + C::kColS + 128u * (j & 1) + 64 * wg;
-      ok = mbar_wait_warp(bar(C::kBarS0 + (j & 1)), (j >> 1) & 1, wctx, kBSiteS);
+      ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
       if (!ok) break;
       if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
       tc_fence_after();
@@ -523,6 +592,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
       tmem_wait_ld(sv[0]);
       reg_tie(sv[1]);
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
       const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
       const int lim = (CAUSAL ? min(q_row, p.N - 1) : p.N - 1) - kvc0;  // last visible column offset
       float pe[64];
@@ -556,80 +627,92 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         fmul2(d0, d1, pe[c], pe[c + 1], t0, t1);
         w[c >> 1] = pack_bf16x2(d0, d1);
       }
-      tmem_st_32x32b_x32(s_tm, w);  // dS (bf16) over the first 32 columns of this warpgroup's S
+      tmem_st_32x32b_x32(ds_tm, w);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarDS));
       if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
     }
-    // ---- epilogue: dQ * scale -> bf16 -> shared (Q tile, free once every S MMA is done) -> TMA store
+    // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
-    uint8_t *stage = smem + C::kOffQ;
+    uint8_t *stage = smem + C::kOffStage;
     if (ok) acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
     fence_proxy_async_smem();
     named_bar_sync(1, 256);
     if (threadIdx.x == 0 && ok) {
-      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffQ + bx * 16384, bx * 64, h, q0, b);
+      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, q0, b);
       bulk_commit();
       bulk_wait_read_all();
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
-    // Order: S_0 | dP_j S_{j+1} [dS_j] dQ_j | ...  S alternates between two
-    // TMEM buffers; S_{j+1} goes into the buffer that held dS_{j-1}, which
-    // dQ_{j-1} (issued earlier, executed in order) has already consumed.
+    // Order: S_0 dP_0 | [S read] S_{j+1} [dS_j] dQ_j dP_{j+1} | ...
+    // S_{j+1} overwrites S_j once the elementwise warps hold it in registers;
+    // dS_j (bf16, over the dP columns) is read by dQ_j, which precedes dP_{j+1}
+    // (the tensor pipe runs one thread's MMAs in order).
     if (lane == 0) {
-      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP
-      constexpr uint32_t id_dq = make_idesc_bf16(128, D, false, true);    // dQ: A = dS in TMEM, B = K MN-major
-      const uint64_t q_d = make_sdesc_sw128(sbase + C::kOffQ, 0, 1024);
-      const uint64_t do_d = make_sdesc_sw128(sbase + C::kOffDO, 0, 1024);
+      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP (A in TMEM, B K-major)
+      constexpr uint32_t id_dq = make_idesc_bf16(128, D, false, true);    // dQ (A = dS in TMEM, B = K MN-major)
       const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
       const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
       auto slot_off = [](int fill) { return (uint64_t)(((fill % C::kStages) * C::kTile) >> 4); };
       auto par = [](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1 (K_j is fill 2j)
+      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      auto issue_s = [&](int j) {  // S_j = Q K_j^T (K_j is fill 2j)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + 128u * (j & 1), q_d + kmaj(kk), ring_d + slot_off(2 * j) + kmaj(kk), id_s, kk > 0);
-        tc_commit(bar(C::kBarS0 + (j & 1)));
+          mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(2 * j) + kmaj(kk), id_s, kk > 0);
+        tc_commit(bar(C::kBarS));
       };
-      bool ok = mbar_wait(bar(C::kBarQ), 0, wctx, kBSiteQ);
+      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T (V_j is fill 2j + 1)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(2 * j + 1) + kmaj(kk), id_s,
+                 kk > 0);
+        tc_commit(bar(C::kBarDP));
+        tc_commit(bar(C::kBarEmpty0 + (2 * j + 1) % C::kStages));  // V_j consumed
+      };
+      bool ok = mbar_wait(bar(C::kBarQdo), 0, wctx, kBSiteQ);
       if (ok) ok = mbar_wait(bar(C::kBarFull0), par(0), wctx, kBSiteFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
+        ok = mbar_wait(bar(C::kBarFull0 + 1 % C::kStages), par(1), wctx, kBSiteFull);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
       }
       for (int j = 0; j < nb && ok; ++j) {
         FA_TRACE_EV(1, j, 8);
-        // dP_j = dO V_j^T  (the dP columns are free: dS_{j-1} has been formed)
-        ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 1) % C::kStages), par(2 * j + 1), wctx, kBSiteFull);
-        if (ok && j > 0) ok = mbar_wait(bar(C::kBarDS), (j - 1) & 1, wctx, kBSiteDS);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, do_d + kmaj(kk), ring_d + slot_off(2 * j + 1) + kmaj(kk), id_s, kk > 0);
-        tc_commit(bar(C::kBarDP));
-        tc_commit(bar(C::kBarEmpty0 + (2 * j + 1) % C::kStages));  // V_j consumed
-        if (j + 1 < nb) {
-          ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 2) % C::kStages), par(2 * j + 2), wctx, kBSiteFull);
+        const bool more = j + 1 < nb;
+        if (more) {
+          ok = mbar_wait(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
+          FA_TRACE_EV(1, j, 12);
+          if (ok) ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 2) % C::kStages), par(2 * j + 2), wctx, kBSiteFull);
           if (!ok) break;
+          FA_TRACE_EV(1, j, 13);
           tc_fence_after();
           issue_s(j + 1);
         }
-        // dQ += dS_j K_j  (A = dS in TMEM: key columns 64w.. at column 64w of buffer j & 1)
         ok = mbar_wait(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
         if (!ok) break;
         FA_TRACE_EV(1, j, 9);
         tc_fence_after();
-        const uint32_t sb = tmem + C::kColS + 128u * (j & 1);
+        // dQ += dS_j K_j
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDQ, sb + 64u * (kk >> 2) + 8u * (kk & 3), ring_mn + slot_off(2 * j) + (uint64_t)(kk * 128),
+          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(2 * j) + (uint64_t)(kk * 128),
                  id_dq, (j > 0 || kk > 0));
         tc_commit(bar(C::kBarEmpty0 + (2 * j) % C::kStages));  // K_j consumed
+        if (more) {
+          ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 3) % C::kStages), par(2 * j + 3), wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(j + 1);
+        }
         FA_TRACE_EV(1, j, 10);
       }
       tc_commit(bar(C::kBarFinal));
@@ -640,15 +723,9 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       }
     }
   } else {
-    // ===================================================== TMA producer
+    // ===================================================== TMA producer: K_j, V_j alternating through the ring
     if (lane == 0) {
-      const uint64_t keep = policy_evict_last();   // K, V are re-read by every query tile
-      const uint64_t once = policy_evict_first();  // Q, dO are read once here
-      mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTile);
-      for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_4d_hint(sbase + C::kOffQ + bx * 16384, &p.tm_q, bar(C::kBarQ), bx * 64, h, q0, b, once);
-        tma_load_4d_hint(sbase + C::kOffDO + bx * 16384, &p.tm_do, bar(C::kBarQ), bx * 64, h, q0, b, once);
-      }
+      const uint64_t keep = policy_evict_last();  // K, V are re-read by every query tile
       bool ok = true;
       int fill = 0;
       for (int j = 0; j < nb && ok; ++j) {
@@ -667,7 +744,6 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       for (int f = max(0, fill - C::kStages); f < fill; ++f)
         while (!mbar_test(bar(C::kBarFull0 + f % C::kStages), (f / C::kStages) & 1) &&
                global_timer_ns() - t0 < kWaitLimitNs) {}
-      while (!mbar_test(bar(C::kBarQ), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   }
 
@@ -706,8 +782,12 @@ int launch_dkdv_t(const BwdParams &p, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 int launch_dq_t(const BwdParams &p, cudaStream_t stream) {
-  return launch_kernel(bwd_dq_kernel<D, CAUSAL>, dim3((p.N + 127) / 128, p.H, p.B), DqCfg<D>::kThreads,
-                       DqCfg<D>::kSmemBytes, p, stream);
+  auto kern = bwd_dq_kernel<D, CAUSAL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes) != cudaSuccess)
+    return FA_ERR_CUDA;
+  kern<<<dim3((p.N + 127) / 128, p.H, p.B), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(
+      p, static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.dO));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
