@@ -211,6 +211,9 @@ def run_ours(args):
     fa.lib()  # fails loudly if the CUDA library is missing
 
     w = workload(args.workload)
+    if args.batch:
+        w = inputs.Workload(w.name.replace(f"B{w.B}", f"B{args.batch}"), args.batch, w.H, w.Hkv, w.N, w.d, w.causal,
+                            w.seed, w.outliers, w.backward)
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     scale, causal = w.sm_scale, w.causal
     xw = inputs.Workload(w.name, B, H, Hkv, N, d, causal, w.seed + 1000 * rank, w.outliers, w.backward)
@@ -335,6 +338,12 @@ def run_ours(args):
     out["clocks"] = clocks
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, D2H outputs every step
+    if args.no_e2e:
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return 0
     pin = {n: x_cpu[n].pin_memory() for n in ("q", "k", "v") + (("dO",) if w.backward else ())}
     outs_d = [o, lse] + ([dq, dk, dv] if w.backward else [])
     outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_d]
@@ -392,6 +401,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["headline", "causal", "gqa"], default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases of the same kernels, e.g. for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, whatever is asked
     return run_reference(args) if args.impl == "reference" else run_ours(args)
