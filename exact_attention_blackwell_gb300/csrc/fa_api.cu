@@ -156,7 +156,6 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
               size_t workspace_bytes) {
   int rc = check_common(B, H, Hkv, N, d, scale);
   if (rc != FA_OK) return rc;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   for (const void *x : {q, k, v, dO, dq, dk, dv})
     if (x && !aligned16(x)) return FA_ERR_ALIGNMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);

@@ -145,6 +145,106 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
   return false;
 }
 
+// Key-row elementwise work of the dK/dV kernels over all iterations: one thread
+// per key row (TMEM lane), warpgroup wg owns query columns [64 wg, 64 wg + 64).
+//   P^T  = 2^(S^T c - LSE2), masked -> registers (fp32) and TMEM over S^T (bf16, dV's A operand)
+//   dS^T = P^T (dP^T - D)            -> TMEM over dP^T (bf16, dK's A operand)
+// C names the barriers, the row ring and the TMEM columns.  Returns false if a wait ran out.
+template <class C, bool CAUSAL>
+__device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *smem, uint32_t bar0, uint32_t tmem,
+                                          const WaitCtx &wctx, int warp, int n_iter, int i_start, int per_head,
+                                          int jt, int kv0) {
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
+  const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;  // S^T columns of this warpgroup
+  const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first 32
+  const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
+  const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
+  const bool row_valid = kv0 + r < p.N;
+  bool ok = true;
+  for (int it = 0; it < n_iter && ok; ++it) {
+    const int rs = it % C::kRowStages;
+    const int i = i_start + it % per_head;
+    const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
+    const float *dlt_s = lse2_s + 128;
+    // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
+    ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
+    if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
+    tc_fence_after();
+    const bool need_mask = !row_valid || (CAUSAL && i == jt);  // key rows past N, or the diagonal tile
+    uint32_t sv[2][32];
+    tmem_ld_32x32b_x32(s_tm, sv[0]);
+    tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+    tmem_wait_ld(sv[0]);
+    reg_tie(sv[1]);
+    float pe[64];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
+        float x[4];
+        ffma2(x[0], x[1], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]), p.scale_log2, p.scale_log2,
+              -l4.x, -l4.y);
+        ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), p.scale_log2,
+              p.scale_log2, -l4.z, -l4.w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
+        if (need_mask) {
+          const int qc = 64 * wg + 32 * c + k;  // query column within tile i
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (!row_valid || qc + u < r) pe[32 * c + k + u] = 0.f;
+        }
+        w[k >> 1] = pack_bf16x2(pe[32 * c + k], pe[32 * c + k + 1]);
+        w[(k >> 1) + 1] = pack_bf16x2(pe[32 * c + k + 2], pe[32 * c + k + 3]);
+      }
+      tmem_st_32x32b_x16(p_tm + 16 * c, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarP));
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
+    // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
+    ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
+    tc_fence_after();
+    uint32_t dpv[2][32];
+    tmem_ld_32x32b_x32(dp_tm, dpv[0]);
+    tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
+    tmem_wait_ld(dpv[0]);
+    reg_tie(dpv[1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + 32 * c + k);
+        float t[4], ds[4];
+        fadd2(t[0], t[1], __uint_as_float(dpv[c][k]), __uint_as_float(dpv[c][k + 1]), -d4.x, -d4.y);
+        fadd2(t[2], t[3], __uint_as_float(dpv[c][k + 2]), __uint_as_float(dpv[c][k + 3]), -d4.z, -d4.w);
+        fmul2(ds[0], ds[1], pe[32 * c + k], pe[32 * c + k + 1], t[0], t[1]);
+        fmul2(ds[2], ds[3], pe[32 * c + k + 2], pe[32 * c + k + 3], t[2], t[3]);
+        w[k >> 1] = pack_bf16x2(ds[0], ds[1]);
+        w[(k >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+      tmem_st_32x32b_x16(ds_tm + 16 * c, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarDS));
+    mbar_arrive(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
+  }
+  return ok;
+}
+
 // ================================================================== dK, dV
 template <int D>
 struct DkdvCfg {
@@ -224,93 +324,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     // P stays in registers (fp32) from its computation to dS; P^T (bf16) goes
     // to TMEM over the S^T columns for the dV MMA, dS^T (bf16) over the dP^T
     // columns once they have been read, for the dK MMA.
-    const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
-    const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;  // S^T columns of this warpgroup
-    const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first 32
-    const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
-    const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
-    const bool row_valid = kv0 + r < p.N;
-    bool ok = true;
-    for (int it = 0; it < n_iter && ok; ++it) {
-      const int rs = it % C::kRowStages;
-      const int i = i_start + it % per_head;
-      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
-      const float *dlt_s = lse2_s + 128;
-      // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
-      ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
-      if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
-      if (!ok) break;
-      if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
-      tc_fence_after();
-      const bool need_mask = !row_valid || (CAUSAL && i == jt);  // key rows past N, or the diagonal tile
-      uint32_t sv[2][32];
-      tmem_ld_32x32b_x32(s_tm, sv[0]);
-      tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
-      tmem_wait_ld(sv[0]);
-      reg_tie(sv[1]);
-      float pe[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
-          float x[4];
-          ffma2(x[0], x[1], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]), p.scale_log2, p.scale_log2,
-                -l4.x, -l4.y);
-          ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), p.scale_log2,
-                p.scale_log2, -l4.z, -l4.w);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
-          if (need_mask) {
-            const int qc = 64 * wg + 32 * c + k;  // query column within tile i
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (!row_valid || qc + u < r) pe[32 * c + k + u] = 0.f;
-          }
-          w[k >> 1] = pack_bf16x2(pe[32 * c + k], pe[32 * c + k + 1]);
-          w[(k >> 1) + 1] = pack_bf16x2(pe[32 * c + k + 2], pe[32 * c + k + 3]);
-        }
-        tmem_st_32x32b_x16(p_tm + 16 * c, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarP));
-      if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
-      // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
-      ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
-      if (!ok) break;
-      if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
-      tc_fence_after();
-      uint32_t dpv[2][32];
-      tmem_ld_32x32b_x32(dp_tm, dpv[0]);
-      tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
-      tmem_wait_ld(dpv[0]);
-      reg_tie(dpv[1]);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + 32 * c + k);
-          float t[4], ds[4];
-          fadd2(t[0], t[1], __uint_as_float(dpv[c][k]), __uint_as_float(dpv[c][k + 1]), -d4.x, -d4.y);
-          fadd2(t[2], t[3], __uint_as_float(dpv[c][k + 2]), __uint_as_float(dpv[c][k + 3]), -d4.z, -d4.w);
-          fmul2(ds[0], ds[1], pe[32 * c + k], pe[32 * c + k + 1], t[0], t[1]);
-          fmul2(ds[2], ds[3], pe[32 * c + k + 2], pe[32 * c + k + 3], t[2], t[3]);
-          w[k >> 1] = pack_bf16x2(ds[0], ds[1]);
-          w[(k >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-        tmem_st_32x32b_x16(ds_tm + 16 * c, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDS));
-      mbar_arrive(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
-      if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
-    }
+    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0);
     // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
     //      drained once every MMA has completed)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
@@ -475,6 +492,74 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   }
 }
 
+// Query-row elementwise work of the dQ kernels over all key tiles: one thread
+// per query row (TMEM lane), warpgroup wg owns key columns [64 wg, 64 wg + 64).
+//   P  = 2^(S c - LSE2), masked -> registers (fp32)
+//   dS = P (dP - D)             -> TMEM over dP (bf16, dQ's A operand)
+template <class C, bool CAUSAL>
+__device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint32_t tmem, const WaitCtx &wctx,
+                                        int warp, int nb, int q_row, float lse2, float dlt) {
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  const int wg = warp >> 2;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;
+  const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
+  const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first 32 of this warpgroup's dP columns
+  bool ok = true;
+  for (int j = 0; j < nb && ok; ++j) {
+    ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
+    tc_fence_after();
+    uint32_t sv[2][32];
+    tmem_ld_32x32b_x32(s_tm, sv[0]);
+    tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+    tmem_wait_ld(sv[0]);
+    reg_tie(sv[1]);
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
+    const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
+    const int lim = (CAUSAL ? min(q_row, p.N - 1) : p.N - 1) - kvc0;  // last visible column offset
+    float pe[64];
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+      float x0, x1;
+      ffma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]), p.scale_log2,
+            p.scale_log2, -lse2, -lse2);
+      pe[c] = ex2_mufu(x0);
+      pe[c + 1] = ex2_mufu(x1);
+    }
+    if (lim < 63) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c > lim) pe[c] = 0.f;
+    }
+    ok = mbar_wait_warp(bar(C::kBarDP), j & 1, wctx, kBSiteDP);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(1, j, 1);
+    tc_fence_after();
+    uint32_t dpv[2][32];
+    tmem_ld_32x32b_x32(dp_tm, dpv[0]);
+    tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
+    tmem_wait_ld(dpv[0]);
+    reg_tie(dpv[1]);
+    uint32_t w[32];
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+      float t0, t1, d0, d1;
+      fadd2(t0, t1, __uint_as_float(dpv[c >> 5][c & 31]), __uint_as_float(dpv[c >> 5][(c & 31) + 1]), -dlt, -dlt);
+      fmul2(d0, d1, pe[c], pe[c + 1], t0, t1);
+      w[c >> 1] = pack_bf16x2(d0, d1);
+    }
+    tmem_st_32x32b_x32(ds_tm, w);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar(C::kBarDS));
+    if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
+  }
+  return ok;
+}
+
 // ================================================================== dQ
 template <int D>
 struct DqCfg {
@@ -545,9 +630,6 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;
-    const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
-    const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first 32 of this warpgroup's dP columns
     const int q_row = q0 + r;
     {
       // Q (warpgroup 0) or dO (warpgroup 1): this thread's row, bf16 pairs in
@@ -581,58 +663,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
     const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
     const float dlt = p.delta[rw];
-    bool ok = true;
-    for (int j = 0; j < nb && ok; ++j) {
-      ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
-      if (!ok) break;
-      if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
-      tc_fence_after();
-      uint32_t sv[2][32];
-      tmem_ld_32x32b_x32(s_tm, sv[0]);
-      tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
-      tmem_wait_ld(sv[0]);
-      reg_tie(sv[1]);
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
-      const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
-      const int lim = (CAUSAL ? min(q_row, p.N - 1) : p.N - 1) - kvc0;  // last visible column offset
-      float pe[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float x0, x1;
-        ffma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]), p.scale_log2,
-              p.scale_log2, -lse2, -lse2);
-        pe[c] = ex2_mufu(x0);
-        pe[c + 1] = ex2_mufu(x1);
-      }
-      if (lim < 63) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c > lim) pe[c] = 0.f;
-      }
-      ok = mbar_wait_warp(bar(C::kBarDP), j & 1, wctx, kBSiteDP);
-      if (!ok) break;
-      if (threadIdx.x == 0) FA_TRACE_EV(1, j, 1);
-      tc_fence_after();
-      uint32_t dpv[2][32];
-      tmem_ld_32x32b_x32(dp_tm, dpv[0]);
-      tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
-      tmem_wait_ld(dpv[0]);
-      reg_tie(dpv[1]);
-      uint32_t w[32];
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float t0, t1, d0, d1;
-        fadd2(t0, t1, __uint_as_float(dpv[c >> 5][c & 31]), __uint_as_float(dpv[c >> 5][(c & 31) + 1]), -dlt, -dlt);
-        fmul2(d0, d1, pe[c], pe[c + 1], t0, t1);
-        w[c >> 1] = pack_bf16x2(d0, d1);
-      }
-      tmem_st_32x32b_x32(ds_tm, w);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDS));
-      if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
-    }
+    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt);
     // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
@@ -755,6 +786,401 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   }
 }
 
+// ================================================================== head dim 256
+// At d = 256, dV and dK alone would fill the 512 TMEM columns and a K, V, Q, dO
+// tile set would not fit in shared memory.  So:
+//  * bwd_dkdv256: one CTA per (key tile, half e of the head dim); it produces
+//    columns [128 e, 128 e + 128) of dV and dK, recomputing S^T and dP^T in
+//    full (TMEM: S^T 128 | dP^T 128 | dV_e 128 | dK_e 128).  K_j and V_j stay in
+//    shared memory; Q_i and dO_i stream as 128-column halves through three
+//    32 KB slots, the half that is only needed for S^T / dP^T first.
+//  * bwd_dq256: one CTA per query tile (TMEM: S 128 | dP 128 | dQ 256); Q_i and
+//    dO_i stay in shared memory; V_j then K_j stream as halves through three
+//    slots, dP_j issued before S_j so that V_j's slots free early.
+template <bool CAUSAL>
+struct Dkdv256Cfg {
+  static constexpr int D = 256;
+  static constexpr int kTile = 128 * D * 2;  // 64 KB
+  static constexpr int kHalf = kTile / 2;    // 32 KB: 128 rows x 128 columns
+  static constexpr int kSlots = 3;
+  static constexpr int kRowStages = 2;
+  static constexpr int kThreads = 320;
+  static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
+  static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kOffK = 0, kOffV = kTile, kOffRing = 2 * kTile;
+  static constexpr int kOffRows = kOffRing + kSlots * kHalf;
+  enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
+         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages, kBarDP, kBarP, kBarDS,
+         kBarFinal, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dkdv256Cfg<CAUSAL>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int jt = blockIdx.x >> 1;  // key/value tile
+  const int e = blockIdx.x & 1;    // half of the head dim this CTA produces
+  const int kh = blockIdx.y, b = blockIdx.z;
+  const int g = p.H / p.Hkv;
+  const int n_q = (p.N + 127) / 128;
+  const int Npad = n_q * 128;
+  const int i_start = CAUSAL ? jt : 0;
+  const int per_head = n_q - i_start;
+  const int n_iter = g * per_head;
+  const int kv0 = jt * 128;
+  // per iteration four fills: Q half (1-e), Q half e, dO half (1-e), dO half e
+  auto fill_of = [&](int it, bool is_do, int half) { return 4 * it + (is_do ? 2 : 0) + (half == e ? 1 : 0); };
+  auto slot_of = [](int fill) { return fill % C::kSlots; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
+      mbar_init(bar(i), all ? 256u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0);
+    // ---- epilogue: warpgroup 0 stores dV[:, half e], warpgroup 1 dK[:, half e] * scale (ring slots 0, 1)
+    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffRing + wg * C::kHalf;
+    if (ok) acc_to_smem<128>(tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK), stage, r, 0, wg == 0 ? 1.0f : p.scale);
+    fence_proxy_async_smem();
+    if (wg == 0) named_bar_sync(1, 128);
+    else named_bar_sync(2, 128);
+    if (r == 0 && ok) {
+      const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+      for (int bx = 0; bx < 2; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, 128 * e + bx * 64, kh, kv0, b);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue: S^T, dP^T, [P] dV_e, [dS] dK_e per iteration
+    if (lane == 0) {
+      constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_out = make_idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major half tile
+      const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
+      const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
+      auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
+      auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kHalf) >> 4); };
+      auto full_ok = [&](int fill) {
+        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
+      };
+      auto release = [&](int fill) { tc_commit(bar(C::kBarEmpty0 + slot_of(fill))); };
+      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      bool ok = mbar_wait(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        // S^T = K Q^T over the full head dim: K steps 0-7 read Q half 0, 8-15 Q half 1
+        ok = full_ok(fill_of(it, false, 0)) && full_ok(fill_of(it, false, 1));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(fill_of(it, false, kk >> 3)) + kmaj(kk & 7), id_kk,
+                 kk > 0);
+        tc_commit(bar(C::kBarS));
+        release(fill_of(it, false, 1 - e));
+        // dP^T = V dO^T
+        ok = full_ok(fill_of(it, true, 0)) && full_ok(fill_of(it, true, 1));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(fill_of(it, true, kk >> 3)) + kmaj(kk & 7), id_kk,
+                 kk > 0);
+        tc_commit(bar(C::kBarDP));
+        release(fill_of(it, true, 1 - e));
+        // dV_e += P^T dO[:, half e]
+        ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t do_mn = ring_mn + soff(fill_of(it, true, e));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), do_mn + (uint64_t)(kk * 128), id_out,
+                 (it > 0 || kk > 0));
+        release(fill_of(it, true, e));
+        // dK_e += dS^T Q[:, half e]
+        ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t q_mn = ring_mn + soff(fill_of(it, false, e));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), q_mn + (uint64_t)(kk * 128), id_out,
+                 (it > 0 || kk > 0));
+        release(fill_of(it, false, e));
+      }
+      tc_commit(bar(C::kBarFinal));
+      tc_commit(bar(C::kBarDrain));
+      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTile);
+      for (int bx = 0; bx < 4; ++bx) {
+        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, kv0, b);
+        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, kv0, b);
+      }
+      bool ok = true;
+      int fill = 0, rows_issued = 0;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int hh = kh * g + it / per_head;
+        const int i = i_start + it % per_head;
+        for (int t = 0; t < 4 && ok; ++t, ++fill) {  // Q(1-e), Q(e), dO(1-e), dO(e)
+          const int half = (t & 1) ? e : 1 - e;
+          const int s = slot_of(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), ((fill / C::kSlots) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          const uint32_t fb = bar(C::kBarFull0 + s);
+          mbar_arrive_expect_tx(fb, C::kHalf);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_hint(sbase + C::kOffRing + s * C::kHalf + bx * 16384, t < 2 ? &p.tm_q : &p.tm_do, fb,
+                             128 * half + bx * 64, hh, i * 128, b, keep);
+        }
+        if (!ok) break;
+        const int rs = it % C::kRowStages;
+        ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
+        if (!ok) break;
+        const uint32_t rb = bar(C::kBarRowFull0 + rs);
+        mbar_arrive_expect_tx(rb, 1024);
+        const size_t roff = ((size_t)b * p.H + hh) * Npad + (size_t)i * 128;
+        const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+        bulk_load(rdst, p.lse2 + roff, 512, rb);
+        bulk_load(rdst + 512, p.delta + roff, 512, rb);
+        ++rows_issued;
+      }
+      const uint64_t t0 = global_timer_ns();
+      for (int f = max(0, fill - C::kSlots); f < fill; ++f)
+        while (!mbar_test(bar(C::kBarFull0 + f % C::kSlots), (f / C::kSlots) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
+        while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_test(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+struct Dq256Cfg {
+  static constexpr int D = 256;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kHalf = kTile / 2;
+  static constexpr int kSlots = 3;
+  static constexpr int kThreads = 320;
+  static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
+  static constexpr int kColS = 0, kColDP = 128, kColDQ = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kOffQ = 0, kOffDO = kTile, kOffRing = 2 * kTile;
+  enum { kBarQdo, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarS = kBarEmpty0 + kSlots, kBarSFree, kBarDP,
+         kBarDS, kBarFinal, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffRing + kSlots * kHalf;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dq256Cfg;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_q = (p.N + 127) / 128;
+  const int it_q = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / (p.H / p.Hkv);
+  const int Npad = n_q * 128;
+  const int q0 = it_q * 128;
+  const int nb = CAUSAL ? it_q + 1 : n_q;
+  // per key tile four fills: V half 0, V half 1, K half 0, K half 1
+  auto fill_of = [](int j, bool is_k, int half) { return 4 * j + (is_k ? 2 : 0) + half; };
+  auto slot_of = [](int fill) { return fill % C::kSlots; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), (i == C::kBarSFree || i == C::kBarDS) ? 256u : 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int q_row = q0 + r;
+    const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
+    const float lse2 = p.lse2[rw];
+    const float dlt = p.delta[rw];
+    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt);
+    // ---- epilogue: dQ * scale -> bf16 -> shared (the Q tile, free once every S MMA is done) -> TMA store
+    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffQ;
+    if (ok) acc_to_smem<128>(tmem + lane_off + C::kColDQ, stage, r, wg * 128, p.scale);
+    fence_proxy_async_smem();
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 0 && ok) {
+      for (int bx = 0; bx < 4; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffQ + bx * 16384, bx * 64, h, q0, b);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue: dP_j, S_j, [dS_j] dQ_j per key tile
+    if (lane == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_dq = make_idesc_bf16(128, 128, false, true);  // A = dS in TMEM, B = K half MN-major
+      const uint64_t q_d = make_sdesc_sw128(sbase + C::kOffQ, 0, 1024);
+      const uint64_t do_d = make_sdesc_sw128(sbase + C::kOffDO, 0, 1024);
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
+      auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
+      auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kHalf) >> 4); };
+      auto full_ok = [&](int fill) {
+        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
+      };
+      auto release = [&](int fill) { tc_commit(bar(C::kBarEmpty0 + slot_of(fill))); };
+      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      bool ok = mbar_wait(bar(C::kBarQdo), 0, wctx, kBSiteQ);
+      for (int j = 0; j < nb && ok; ++j) {
+        // dP_j = dO V_j^T (the dP columns are free: dQ_{j-1} has read dS_{j-1} from them)
+        ok = full_ok(fill_of(j, false, 0)) && full_ok(fill_of(j, false, 1));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          mma_ss(tmem + C::kColDP, do_d + kmaj(kk), ring_d + soff(fill_of(j, false, kk >> 3)) + kmaj(kk & 7), id_s,
+                 kk > 0);
+        tc_commit(bar(C::kBarDP));
+        release(fill_of(j, false, 0));
+        release(fill_of(j, false, 1));
+        // S_j = Q K_j^T (the S columns are free: S_{j-1} was read before dS_{j-1})
+        ok = full_ok(fill_of(j, true, 0)) && full_ok(fill_of(j, true, 1));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          mma_ss(tmem + C::kColS, q_d + kmaj(kk), ring_d + soff(fill_of(j, true, kk >> 3)) + kmaj(kk & 7), id_s,
+                 kk > 0);
+        tc_commit(bar(C::kBarS));
+        // dQ[:, half] += dS_j K_j[:, half]
+        ok = mbar_wait(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDQ + 128u * half, tmem + C::kColDP + a_col(kk),
+                   ring_mn + soff(fill_of(j, true, half)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
+        release(fill_of(j, true, 0));
+        release(fill_of(j, true, 1));
+      }
+      tc_commit(bar(C::kBarFinal));
+      tc_commit(bar(C::kBarDrain));
+      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint64_t once = policy_evict_first();
+      mbar_arrive_expect_tx(bar(C::kBarQdo), 2 * C::kTile);
+      for (int bx = 0; bx < 4; ++bx) {
+        tma_load_4d_hint(sbase + C::kOffQ + bx * 16384, &p.tm_q, bar(C::kBarQdo), bx * 64, h, q0, b, once);
+        tma_load_4d_hint(sbase + C::kOffDO + bx * 16384, &p.tm_do, bar(C::kBarQdo), bx * 64, h, q0, b, once);
+      }
+      bool ok = true;
+      int fill = 0;
+      for (int j = 0; j < nb && ok; ++j) {
+        for (int t = 0; t < 4 && ok; ++t, ++fill) {  // V0, V1, K0, K1
+          const int s = slot_of(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), ((fill / C::kSlots) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          const uint32_t fb = bar(C::kBarFull0 + s);
+          mbar_arrive_expect_tx(fb, C::kHalf);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_hint(sbase + C::kOffRing + s * C::kHalf + bx * 16384, t < 2 ? &p.tm_v : &p.tm_k, fb,
+                             128 * (t & 1) + bx * 64, kh, j * 128, b, keep);
+        }
+      }
+      const uint64_t t0 = global_timer_ns();
+      for (int f = max(0, fill - C::kSlots); f < fill; ++f)
+        while (!mbar_test(bar(C::kBarFull0 + f % C::kSlots), (f / C::kSlots) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      while (!mbar_test(bar(C::kBarQdo), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ launches
 template <typename Kern>
 int launch_kernel(Kern kern, dim3 grid, int threads, int smem, const BwdParams &p, cudaStream_t stream) {
@@ -796,6 +1222,7 @@ int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, con
   switch (d) {
     case 64: return launch_pre_t<64>(p, o, dO, lse, stream);
     case 128: return launch_pre_t<128>(p, o, dO, lse, stream);
+    case 256: return launch_pre_t<256>(p, o, dO, lse, stream);
     default: return FA_ERR_UNSUPPORTED;
   }
 }
@@ -804,6 +1231,11 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
   switch (d) {
     case 64: return causal ? launch_dkdv_t<64, true>(p, stream) : launch_dkdv_t<64, false>(p, stream);
     case 128: return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
+    case 256: {
+      const dim3 grid(2 * ((p.N + 127) / 128), p.Hkv, p.B);  // x: (key tile, head-dim half)
+      return causal ? launch_kernel(bwd_dkdv256_kernel<true>, grid, Dkdv256Cfg<true>::kThreads, Dkdv256Cfg<true>::kSmemBytes, p, stream)
+                    : launch_kernel(bwd_dkdv256_kernel<false>, grid, Dkdv256Cfg<false>::kThreads, Dkdv256Cfg<false>::kSmemBytes, p, stream);
+    }
     default: return FA_ERR_UNSUPPORTED;
   }
 }
@@ -812,6 +1244,11 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
   switch (d) {
     case 64: return causal ? launch_dq_t<64, true>(p, stream) : launch_dq_t<64, false>(p, stream);
     case 128: return causal ? launch_dq_t<128, true>(p, stream) : launch_dq_t<128, false>(p, stream);
+    case 256: {
+      const dim3 grid((p.N + 127) / 128, p.H, p.B);
+      return causal ? launch_kernel(bwd_dq256_kernel<true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, p, stream)
+                    : launch_kernel(bwd_dq256_kernel<false>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, p, stream);
+    }
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -71,8 +71,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d);
 
 /* Backward pass.  Inputs q, k, v, o, lse from the forward, and dO [B,N,H,d].
- * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  Head dims 64 and 128
- * (d = 256 returns FA_ERR_UNSUPPORTED).  `workspace` is caller owned device
+ * Writes dq [B,N,H,d], dk and dv [B,N,Hkv,d] (bf16).  `workspace` is caller owned device
  * memory of at least fa_bwd_workspace_bytes() bytes, 256-byte aligned; its
  * contents on entry do not matter and are overwritten.  No atomics: results
  * are bitwise reproducible for the same inputs. */

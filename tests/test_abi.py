@@ -96,7 +96,7 @@ def test_bwd_stages_reject_bad_arguments(lib):
     assert fa.fa_bwd_prepare(A, A + 2, A, 1, 2, 2, 256, 128, A, nb, 0) == fa.FA_ERR_ALIGNMENT
     assert fa.fa_bwd_prepare(A, A, A, 1, 2, 2, 256, 128, A, nb - 4, 0) == fa.FA_ERR_WORKSPACE
     assert fa.fa_bwd_dkdv(A, A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd_dkdv(A, A, A, A, A, A, 1, 2, 2, 256, 256, 0.1, 0, A, nb, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_dkdv(A, A, A, A, A, A, 1, 2, 2, 256, 96, 0.1, 0, A, nb, 0) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd_dkdv(A, A, A, A, A + 8, A, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_ALIGNMENT
     assert fa.fa_bwd_dq(A, A, A, A, None, 1, 2, 2, 256, 128, 0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_bwd_dq(A, A, A, A, A, 1, 2, 2, 256, 128, -0.1, 0, A, nb, 0) == fa.FA_ERR_INVALID_ARG

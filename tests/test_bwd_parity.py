@@ -68,6 +68,9 @@ CASES = [
     (1, 256, 2, 2, 64, False),
     (1, 395, 2, 2, 64, True),
     (2, 200, 4, 2, 64, True),
+    (1, 256, 2, 2, 256, False),
+    (1, 333, 2, 1, 256, True),
+    (2, 128, 2, 2, 256, True),
 ]
 
 
