@@ -197,7 +197,7 @@ def run_ours(args):
     import torch
 
     import exact_attention_blackwell_gb300 as fa
-    from exact_attention_blackwell_gb300 import inputs
+    from exact_attention_blackwell_gb300 import inputs, sharding
 
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
@@ -216,7 +216,7 @@ def run_ours(args):
                             w.seed, w.outliers, w.backward)
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     scale, causal = w.sm_scale, w.causal
-    xw = inputs.Workload(w.name, B, H, Hkv, N, d, causal, w.seed + 1000 * rank, w.outliers, w.backward)
+    xw = inputs.Workload(w.name, B, H, Hkv, N, d, causal, sharding.rank_seed(w.seed, rank), w.outliers, w.backward)
     x_cpu = inputs.make_inputs(xw, with_dO=w.backward)
     dev = torch.device("cuda", local)
     q, k, v = (x_cpu[n].to(dev) for n in ("q", "k", "v"))
@@ -281,11 +281,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = sharding.max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     if fa.fa_last_device_status(sptr) != fa.FA_OK:
         raise RuntimeError("device status reports a timed-out wait")
     if not torch.isfinite(o).all() or (w.backward and not torch.isfinite(dq.float()).all()):
@@ -295,7 +291,7 @@ def run_ours(args):
     bwd_f = w.bwd_flops() if w.backward else 0.0
     step_f = fwd_f + bwd_f
     ms_step = total_ms / args.steps
-    value = world * step_f * args.steps / (total_ms * 1e-3) / 1e12
+    value = sharding.whole_job_tflops(step_f, args.steps, total_ms, world)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
     peaks = measured_peaks()
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -366,12 +362,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    out["e2e"] = {"value": world * step_f * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e_ms = sharding.max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    out["e2e"] = {"value": sharding.whole_job_tflops(step_f, e2e_steps, e2e_ms, world), "unit": "TFLOP/s",
                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h),
                   "ms_per_step": e2e_ms / e2e_steps}
