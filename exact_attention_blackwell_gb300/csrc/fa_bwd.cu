@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     // columns) is read by dK_i, which precedes dP_{i+1}: the tensor pipe runs
     // one thread's MMAs in order.  The elementwise warps have loaded S^T_i and
     // dP^T_i into registers before they signal P_i and dS_i.
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; the elected lane issues.
+    {
       constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t id_dv = make_idesc_bf16(128, D, false, true);     // dV, dK (A in TMEM, B MN-major)
       const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
@@ -361,24 +362,31 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       auto slot_of = [](int fill) { return fill % C::kSlots; };
       auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kTile) >> 4); };
       auto full_ok = [&](int fill) {
-        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
+        return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx,
+                              kBSiteFull);
       };
       auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it)
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
-        tc_commit(bar(C::kBarS));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
+          tc_commit(bar(C::kBarS));
+        }
+        __syncwarp();
       };
       auto issue_dp = [&](int it) {  // dP^T = V dO^T   (dO_it is fill 2 it + 1)
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj(kk), id_kk, kk > 0);
-        tc_commit(bar(C::kBarDP));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj(kk), id_kk, kk > 0);
+          tc_commit(bar(C::kBarDP));
+        }
+        __syncwarp();
       };
       // A operand in TMEM: the query columns 64w.. of warpgroup w start at
       // column 64w of the region; 16 query rows per K step = 8 columns.
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
-      bool ok = mbar_wait(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      bool ok = mbar_wait_warp(bar(C::kBarKV), 0, wctx, kBSiteKV);
       if (ok) ok = full_ok(0);
       if (ok) {
         tc_fence_after();
@@ -392,16 +400,19 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       for (int it = 0; it < n_iter && ok; ++it) {
         const bool more = it + 1 < n_iter;
         FA_TRACE_EV(0, it, 8);
-        ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        ok = mbar_wait_warp(bar(C::kBarP), it & 1, wctx, kBSiteP);
         if (!ok) break;
         FA_TRACE_EV(0, it, 9);
         tc_fence_after();
         // dV += P^T dO_it
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
-                 id_dv, (it > 0 || kk > 0));
-        tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
+                   id_dv, (it > 0 || kk > 0));
+          tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
+        }
+        __syncwarp();
         if (more) {
           FA_TRACE_EV(0, it, 12);
           ok = full_ok(2 * it + 2);
@@ -410,16 +421,19 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
           tc_fence_after();
           issue_s(it + 1);
         }
-        ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+        ok = mbar_wait_warp(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
         FA_TRACE_EV(0, it, 10);
         tc_fence_after();
         // dK += dS^T Q_it
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128), id_dv,
-                 (it > 0 || kk > 0));
-        tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it)));  // Q_it consumed (S_it, dK_it)
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128),
+                   id_dv, (it > 0 || kk > 0));
+          tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it)));  // Q_it consumed (S_it, dK_it)
+        }
+        __syncwarp();
         if (more) {
           ok = full_ok(2 * it + 3);
           if (!ok) break;
@@ -428,9 +442,12 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
         }
         FA_TRACE_EV(0, it, 11);
       }
-      tc_commit(bar(C::kBarFinal));
-      tc_commit(bar(C::kBarDrain));
-      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+      if (elect_one()) {
+        tc_commit(bar(C::kBarFinal));
+        tc_commit(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
@@ -681,8 +698,9 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     // Order: S_0 dP_0 | [S read] S_{j+1} [dS_j] dQ_j dP_{j+1} | ...
     // S_{j+1} overwrites S_j once the elementwise warps hold it in registers;
     // dS_j (bf16, over the dP columns) is read by dQ_j, which precedes dP_{j+1}
-    // (the tensor pipe runs one thread's MMAs in order).
-    if (lane == 0) {
+    // (the tensor pipe runs one thread's MMAs in order).  The whole warp runs
+    // the loop and waits; the elected lane issues.
+    {
       constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP (A in TMEM, B K-major)
       constexpr uint32_t id_dq = make_idesc_bf16(128, D, false, true);    // dQ (A = dS in TMEM, B = K MN-major)
       const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
@@ -692,25 +710,31 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       auto par = [](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
       auto issue_s = [&](int j) {  // S_j = Q K_j^T (K_j is fill 2j)
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(2 * j) + kmaj(kk), id_s, kk > 0);
-        tc_commit(bar(C::kBarS));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(2 * j) + kmaj(kk), id_s, kk > 0);
+          tc_commit(bar(C::kBarS));
+        }
+        __syncwarp();
       };
       auto issue_dp = [&](int j) {  // dP_j = dO V_j^T (V_j is fill 2j + 1)
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(2 * j + 1) + kmaj(kk), id_s,
-                 kk > 0);
-        tc_commit(bar(C::kBarDP));
-        tc_commit(bar(C::kBarEmpty0 + (2 * j + 1) % C::kStages));  // V_j consumed
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(2 * j + 1) + kmaj(kk), id_s,
+                   kk > 0);
+          tc_commit(bar(C::kBarDP));
+          tc_commit(bar(C::kBarEmpty0 + (2 * j + 1) % C::kStages));  // V_j consumed
+        }
+        __syncwarp();
       };
-      bool ok = mbar_wait(bar(C::kBarQdo), 0, wctx, kBSiteQ);
-      if (ok) ok = mbar_wait(bar(C::kBarFull0), par(0), wctx, kBSiteFull);
+      bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
+      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0), par(0), wctx, kBSiteFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        ok = mbar_wait(bar(C::kBarFull0 + 1 % C::kStages), par(1), wctx, kBSiteFull);
+        ok = mbar_wait_warp(bar(C::kBarFull0 + 1 % C::kStages), par(1), wctx, kBSiteFull);
       }
       if (ok) {
         tc_fence_after();
@@ -720,35 +744,41 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         FA_TRACE_EV(1, j, 8);
         const bool more = j + 1 < nb;
         if (more) {
-          ok = mbar_wait(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
+          ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
           FA_TRACE_EV(1, j, 12);
-          if (ok) ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 2) % C::kStages), par(2 * j + 2), wctx, kBSiteFull);
+          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + (2 * j + 2) % C::kStages), par(2 * j + 2), wctx, kBSiteFull);
           if (!ok) break;
           FA_TRACE_EV(1, j, 13);
           tc_fence_after();
           issue_s(j + 1);
         }
-        ok = mbar_wait(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
+        ok = mbar_wait_warp(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
         if (!ok) break;
         FA_TRACE_EV(1, j, 9);
         tc_fence_after();
         // dQ += dS_j K_j
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(2 * j) + (uint64_t)(kk * 128),
-                 id_dq, (j > 0 || kk > 0));
-        tc_commit(bar(C::kBarEmpty0 + (2 * j) % C::kStages));  // K_j consumed
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(2 * j) + (uint64_t)(kk * 128),
+                   id_dq, (j > 0 || kk > 0));
+          tc_commit(bar(C::kBarEmpty0 + (2 * j) % C::kStages));  // K_j consumed
+        }
+        __syncwarp();
         if (more) {
-          ok = mbar_wait(bar(C::kBarFull0 + (2 * j + 3) % C::kStages), par(2 * j + 3), wctx, kBSiteFull);
+          ok = mbar_wait_warp(bar(C::kBarFull0 + (2 * j + 3) % C::kStages), par(2 * j + 3), wctx, kBSiteFull);
           if (!ok) break;
           tc_fence_after();
           issue_dp(j + 1);
         }
         FA_TRACE_EV(1, j, 10);
       }
-      tc_commit(bar(C::kBarFinal));
-      tc_commit(bar(C::kBarDrain));
-      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+      if (elect_one()) {
+        tc_commit(bar(C::kBarFinal));
+        tc_commit(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
@@ -885,7 +915,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue: S^T, dP^T, [P] dV_e, [dS] dK_e per iteration
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; the elected lane issues.
+    {
       constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_out = make_idesc_bf16(128, 128, false, true);  // A in TMEM, B MN-major half tile
       const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
@@ -895,56 +926,72 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
       auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kHalf) >> 4); };
       auto full_ok = [&](int fill) {
-        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
+        return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx,
+                              kBSiteFull);
       };
       auto release = [&](int fill) { tc_commit(bar(C::kBarEmpty0 + slot_of(fill))); };
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
-      bool ok = mbar_wait(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      bool ok = mbar_wait_warp(bar(C::kBarKV), 0, wctx, kBSiteKV);
       for (int it = 0; it < n_iter && ok; ++it) {
         // S^T = K Q^T over the full head dim: K steps 0-7 read Q half 0, 8-15 Q half 1
         ok = full_ok(fill_of(it, false, 0)) && full_ok(fill_of(it, false, 1));
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(fill_of(it, false, kk >> 3)) + kmaj(kk & 7), id_kk,
-                 kk > 0);
-        tc_commit(bar(C::kBarS));
-        release(fill_of(it, false, 1 - e));
+          for (int kk = 0; kk < 16; ++kk)
+            mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(fill_of(it, false, kk >> 3)) + kmaj(kk & 7), id_kk,
+                   kk > 0);
+          tc_commit(bar(C::kBarS));
+          release(fill_of(it, false, 1 - e));
+        }
+        __syncwarp();
         // dP^T = V dO^T
         ok = full_ok(fill_of(it, true, 0)) && full_ok(fill_of(it, true, 1));
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(fill_of(it, true, kk >> 3)) + kmaj(kk & 7), id_kk,
-                 kk > 0);
-        tc_commit(bar(C::kBarDP));
-        release(fill_of(it, true, 1 - e));
+          for (int kk = 0; kk < 16; ++kk)
+            mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(fill_of(it, true, kk >> 3)) + kmaj(kk & 7), id_kk,
+                   kk > 0);
+          tc_commit(bar(C::kBarDP));
+          release(fill_of(it, true, 1 - e));
+        }
+        __syncwarp();
         // dV_e += P^T dO[:, half e]
-        ok = mbar_wait(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        ok = mbar_wait_warp(bar(C::kBarP), it & 1, wctx, kBSiteP);
         if (!ok) break;
         tc_fence_after();
         const uint64_t do_mn = ring_mn + soff(fill_of(it, true, e));
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), do_mn + (uint64_t)(kk * 128), id_out,
-                 (it > 0 || kk > 0));
-        release(fill_of(it, true, e));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), do_mn + (uint64_t)(kk * 128), id_out,
+                   (it > 0 || kk > 0));
+          release(fill_of(it, true, e));
+        }
+        __syncwarp();
         // dK_e += dS^T Q[:, half e]
-        ok = mbar_wait(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+        ok = mbar_wait_warp(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
         tc_fence_after();
         const uint64_t q_mn = ring_mn + soff(fill_of(it, false, e));
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), q_mn + (uint64_t)(kk * 128), id_out,
-                 (it > 0 || kk > 0));
-        release(fill_of(it, false, e));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), q_mn + (uint64_t)(kk * 128), id_out,
+                   (it > 0 || kk > 0));
+          release(fill_of(it, false, e));
+        }
+        __syncwarp();
       }
-      tc_commit(bar(C::kBarFinal));
-      tc_commit(bar(C::kBarDrain));
-      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+      if (elect_one()) {
+        tc_commit(bar(C::kBarFinal));
+        tc_commit(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }
@@ -1085,7 +1132,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue: dP_j, S_j, [dS_j] dQ_j per key tile
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; the elected lane issues.
+    {
       constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_dq = make_idesc_bf16(128, 128, false, true);  // A = dS in TMEM, B = K half MN-major
       const uint64_t q_d = make_sdesc_sw128(sbase + C::kOffQ, 0, 1024);
@@ -1095,48 +1143,61 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
       auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kHalf) >> 4); };
       auto full_ok = [&](int fill) {
-        return mbar_wait(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx, kBSiteFull);
+        return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx,
+                              kBSiteFull);
       };
       auto release = [&](int fill) { tc_commit(bar(C::kBarEmpty0 + slot_of(fill))); };
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
-      bool ok = mbar_wait(bar(C::kBarQdo), 0, wctx, kBSiteQ);
+      bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
       for (int j = 0; j < nb && ok; ++j) {
         // dP_j = dO V_j^T (the dP columns are free: dQ_{j-1} has read dS_{j-1} from them)
         ok = full_ok(fill_of(j, false, 0)) && full_ok(fill_of(j, false, 1));
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem + C::kColDP, do_d + kmaj(kk), ring_d + soff(fill_of(j, false, kk >> 3)) + kmaj(kk & 7), id_s,
-                 kk > 0);
-        tc_commit(bar(C::kBarDP));
-        release(fill_of(j, false, 0));
-        release(fill_of(j, false, 1));
+          for (int kk = 0; kk < 16; ++kk)
+            mma_ss(tmem + C::kColDP, do_d + kmaj(kk), ring_d + soff(fill_of(j, false, kk >> 3)) + kmaj(kk & 7), id_s,
+                   kk > 0);
+          tc_commit(bar(C::kBarDP));
+          release(fill_of(j, false, 0));
+          release(fill_of(j, false, 1));
+        }
+        __syncwarp();
         // S_j = Q K_j^T (the S columns are free: S_{j-1} was read before dS_{j-1})
         ok = full_ok(fill_of(j, true, 0)) && full_ok(fill_of(j, true, 1));
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem + C::kColS, q_d + kmaj(kk), ring_d + soff(fill_of(j, true, kk >> 3)) + kmaj(kk & 7), id_s,
-                 kk > 0);
-        tc_commit(bar(C::kBarS));
+          for (int kk = 0; kk < 16; ++kk)
+            mma_ss(tmem + C::kColS, q_d + kmaj(kk), ring_d + soff(fill_of(j, true, kk >> 3)) + kmaj(kk & 7), id_s,
+                   kk > 0);
+          tc_commit(bar(C::kBarS));
+        }
+        __syncwarp();
         // dQ[:, half] += dS_j K_j[:, half]
-        ok = mbar_wait(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
+        ok = mbar_wait_warp(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
         if (!ok) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
+          for (int half = 0; half < 2; ++half)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDQ + 128u * half, tmem + C::kColDP + a_col(kk),
-                   ring_mn + soff(fill_of(j, true, half)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
-        release(fill_of(j, true, 0));
-        release(fill_of(j, true, 1));
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::kColDQ + 128u * half, tmem + C::kColDP + a_col(kk),
+                     ring_mn + soff(fill_of(j, true, half)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
+          release(fill_of(j, true, 0));
+          release(fill_of(j, true, 1));
+        }
+        __syncwarp();
       }
-      tc_commit(bar(C::kBarFinal));
-      tc_commit(bar(C::kBarDrain));
-      if (!mbar_wait(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+      if (elect_one()) {
+        tc_commit(bar(C::kBarFinal));
+        tc_commit(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }

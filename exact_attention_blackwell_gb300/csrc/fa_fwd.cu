@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
     if (rescales) atomicAdd(p.status + 2, rescales);
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; the elected lane issues.
+    {
       constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, D, false, true);
       const uint32_t q_smem = sbase + C::kOffQ;
@@ -317,51 +318,63 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
                  (acc || kk > 0));
       };
       bool ok = nb_max > 0;
-      if (ok) ok = mbar_wait(q_bar, 0, wctx, kSiteQ);
-      if (ok) ok = mbar_wait(full_bar(slot_of(0)), par_of(0), wctx, kSiteKFull);
+      if (ok) ok = mbar_wait_warp(q_bar, 0, wctx, kSiteQ);
+      if (ok) ok = mbar_wait_warp(full_bar(slot_of(0)), par_of(0), wctx, kSiteKFull);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < QT; ++t)
-          if (nb[t] > 0) {
-            issue_s(t, slot_of(0));
-            tc_commit(s_bar(t));
-          }
-        tc_commit(empty_bar(slot_of(0)));
+        if (elect_one()) {
+          for (int t = 0; t < QT; ++t)
+            if (nb[t] > 0) {
+              issue_s(t, slot_of(0));
+              tc_commit(s_bar(t));
+            }
+          tc_commit(empty_bar(slot_of(0)));
+        }
+        __syncwarp();
       }
       for (int j = 0; j < nb_max && ok; ++j) {
         const int fv = 2 * j + 1, fk = 2 * j + 2;
-        ok = mbar_wait(full_bar(slot_of(fv)), par_of(fv), wctx, kSiteVFull);
+        ok = mbar_wait_warp(full_bar(slot_of(fv)), par_of(fv), wctx, kSiteVFull);
         if (!ok) break;
         tc_fence_after();
         bool k_next = false;
         for (int t = 0; t < QT && ok; ++t) {
           if (j >= nb[t]) continue;
-          ok = mbar_wait(p_bar(t), j & 1, wctx, kSitePFull);
+          ok = mbar_wait_warp(p_bar(t), j & 1, wctx, kSitePFull);
           if (!ok) break;
           FA_TRACE_EV(j, 8 + 2 * t);
           tc_fence_after();
-          issue_pv(t, slot_of(fv), j > 0);
+          if (elect_one()) issue_pv(t, slot_of(fv), j > 0);
+          __syncwarp();
           if (j + 1 < nb[t]) {
             if (!k_next) {
-              ok = mbar_wait(full_bar(slot_of(fk)), par_of(fk), wctx, kSiteKFull);
+              ok = mbar_wait_warp(full_bar(slot_of(fk)), par_of(fk), wctx, kSiteKFull);
               if (!ok) break;
               tc_fence_after();
               k_next = true;
             }
-            issue_s(t, slot_of(fk));
-            tc_commit(s_bar(t));
+            if (elect_one()) {
+              issue_s(t, slot_of(fk));
+              tc_commit(s_bar(t));
+            }
+            __syncwarp();
             FA_TRACE_EV(j, 9 + 2 * t);
           } else {
-            tc_commit(o_bar(t));
+            if (elect_one()) tc_commit(o_bar(t));
+            __syncwarp();
           }
         }
-        tc_commit(empty_bar(slot_of(fv)));
-        if (k_next) tc_commit(empty_bar(slot_of(fk)));
+        if (elect_one()) {
+          tc_commit(empty_bar(slot_of(fv)));
+          if (k_next) tc_commit(empty_bar(slot_of(fk)));
+        }
+        __syncwarp();
       }
       // Drain: every MMA this thread issued completes before TMEM is released.
-      tc_commit(drain_bar);
+      if (elect_one()) tc_commit(drain_bar);
+      __syncwarp();
       WaitCtx drain_ctx{abort_flag, p.status};
-      if (!mbar_wait(drain_bar, 0, drain_ctx, kSiteDrain) && *abort_flag) {
+      if (!mbar_wait_warp(drain_bar, 0, drain_ctx, kSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();  // aborted: still give in-flight MMAs time to land
         while (!mbar_test(drain_bar, 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
       }

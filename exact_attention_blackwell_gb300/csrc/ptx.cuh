@@ -27,6 +27,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// One lane of a converged warp (the same lane every time for the same full
+// mask).  The MMA warps run their whole loop warp-wide and issue each group of
+// tcgen05 instructions from the elected lane: with the issue code, descriptor
+// arithmetic and barrier waits warp-uniform, back-to-back MMA groups keep the
+// tensor pipe fed; a single-lane loop with a barrier wait between groups left
+// it idle for about 100 cycles per group on sm_103a.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
