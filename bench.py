@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import datetime
 import hashlib
 import io
 import json
@@ -51,23 +52,39 @@ def env_int(k, default):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock, power and throttle reasons.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Sampling starts before the warm-up (nvidia-smi takes a moment to start);
+    only the readings whose timestamps fall inside the timed window count.
+    """
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock bounds (time.time()) of the timed region."""
+        self.window = (t0, t1)
+
+    @staticmethod
+    def _stamp(text: str):
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -78,24 +95,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for row in csv.reader(io.StringIO(out)):
-            if len(row) < 9:
+            if len(row) < 10:
                 continue
             try:
-                sm.append(float(row[1]))
-                smax.append(float(row[2]))
-                power.append(float(row[3]))
+                rows.append((self._stamp(row[0]), float(row[2]), float(row[3]), float(row[4]), row[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, row[5:9]):
+        inside = [r for r in rows if self.window and r[0] is not None and self.window[0] <= r[0] <= self.window[1]]
+        used = inside if len(inside) >= 3 else rows
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, c, cmax, pw, flags in used:
+            sm.append(c)
+            smax.append(cmax)
+            power.append(pw)
+            for n, v in zip(names, flags):
                 if v.strip().lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "power_w_median": statistics.median(power), "samples": len(sm),
+                "window": "timed region" if used is inside else "whole run (too few samples inside the timed region)",
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ peaks and profiles
@@ -259,6 +283,8 @@ def run_ours(args):
                                                         ws_bytes, sptr)), "fa_bwd_dq")
 
     launches_per_step = 4 if w.backward else 1
+    sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -268,15 +294,14 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take its first reading
     t_start, t_end = ev(), ev()
+    wall0 = time.time()
     t_start.record(stream)
     for _ in range(args.steps):
         step(record=True)
     t_end.record(stream)
     torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -388,7 +413,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 100 for our arm, 20 for the CPU oracle arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["headline", "causal", "gqa"], default="headline")
@@ -398,6 +424,10 @@ def main():
                     help="override the workload's batch (smaller cases of the same kernels, e.g. for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, whatever is asked
+    if args.steps is None:
+        # our arm: about 0.6 s of timed work on the headline workload, long enough for the
+        # clock record; the oracle arm: one (batch, head) slice per step, a few seconds each
+        args.steps = 20 if args.impl == "reference" else 100
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 
