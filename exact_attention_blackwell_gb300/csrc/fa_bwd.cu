@@ -43,7 +43,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ unsigned long long g_trace[2][64][16];
 #define FA_TRACE_EV(k, it, ev)                                                                   \
   do {                                                                                           \
-    if (blockIdx.x == FA_TRACE_CTA && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 64)           \
+    if (blockIdx.x == FA_TRACE_CTA && (it) < 64)                                                \
       g_trace[(k)][(it)][(ev)] = clock64();                                                      \
   } while (0)
 #else
@@ -286,8 +286,11 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int jt = blockIdx.x;  // key/value tile
-  const int kh = blockIdx.y, b = blockIdx.z;
+  const int n_kv = (p.N + 127) / 128;
+  int rank, head;
+  work_order((int)blockIdx.x, n_kv, p.B * p.Hkv, p.sched_chunk, rank, head);
+  const int jt = rank;  // key/value tile; causal: tile 0 sees the most query tiles
+  const int kh = head % p.Hkv, b = head / p.Hkv;
   const int g = p.H / p.Hkv;
   const int n_q = (p.N + 127) / 128;
   const int Npad = n_q * 128;
@@ -615,8 +618,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_q = (p.N + 127) / 128;
-  const int it_q = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // heaviest first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, head;
+  work_order((int)blockIdx.x, n_q, p.B * p.H, p.sched_chunk, rank, head);
+  const int it_q = CAUSAL ? n_q - 1 - rank : rank;  // causal: the longest query rows first
+  const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
   const int Npad = n_q * 128;
   const int q0 = it_q * 128;
@@ -863,9 +868,11 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int jt = blockIdx.x >> 1;  // key/value tile
-  const int e = blockIdx.x & 1;    // half of the head dim this CTA produces
-  const int kh = blockIdx.y, b = blockIdx.z;
+  int rank, head;
+  work_order((int)blockIdx.x, 2 * ((p.N + 127) / 128), p.B * p.Hkv, p.sched_chunk, rank, head);
+  const int jt = rank >> 1;  // key/value tile
+  const int e = rank & 1;    // half of the head dim this CTA produces
+  const int kh = head % p.Hkv, b = head / p.Hkv;
   const int g = p.H / p.Hkv;
   const int n_q = (p.N + 127) / 128;
   const int Npad = n_q * 128;
@@ -1085,8 +1092,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_q = (p.N + 127) / 128;
-  const int it_q = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, head;
+  work_order((int)blockIdx.x, n_q, p.B * p.H, p.sched_chunk, rank, head);
+  const int it_q = CAUSAL ? n_q - 1 - rank : rank;
+  const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
   const int Npad = n_q * 128;
   const int q0 = it_q * 128;
@@ -1261,18 +1270,47 @@ int launch_pre_t(const BwdParams &p, const void *o, const void *dO, const float 
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D, bool CAUSAL>
-int launch_dkdv_t(const BwdParams &p, cudaStream_t stream) {
-  return launch_kernel(bwd_dkdv_kernel<D, CAUSAL>, dim3((p.N + 127) / 128, p.Hkv, p.B), DkdvCfg<D>::kThreads,
-                       DkdvCfg<D>::kSmemBytes, p, stream);
+// Scheduling chunk of the key/value-stationary kernels: Q and dO of every
+// query head of a kv group are re-read by each key tile of the group.
+BwdParams with_kv_order(const BwdParams &p_in, bool causal, int d) {
+  BwdParams p = p_in;
+  const int g = p.H / p.Hkv;
+  p.sched_chunk = sched_chunk_for(causal, (size_t)g * 2 * p.N * d * 2, p.B * p.Hkv);
+  return p;
+}
+
+// Scheduling chunk of the query-stationary kernels: K and V of a kv head are
+// re-read by each query tile of its query heads (kept together in a chunk).
+BwdParams with_q_order(const BwdParams &p_in, bool causal, int d) {
+  BwdParams p = p_in;
+  const int g = p.H / p.Hkv;
+  p.sched_chunk = causal ? g * sched_chunk_for(true, (size_t)2 * p.N * d * 2, p.B * p.Hkv) : 1;
+  return p;
+}
+
+unsigned grid_1d(long long n_tiles, long long n_heads) {
+  const long long n = n_tiles * n_heads;
+  return n > 0x7fffffffLL ? 0u : (unsigned)n;  // 0: too many CTAs for a 1-D grid
 }
 
 template <int D, bool CAUSAL>
-int launch_dq_t(const BwdParams &p, cudaStream_t stream) {
+int launch_dkdv_t(const BwdParams &p_in, cudaStream_t stream) {
+  const BwdParams p = with_kv_order(p_in, CAUSAL, D);
+  const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.Hkv);
+  if (!grid) return FA_ERR_UNSUPPORTED;
+  return launch_kernel(bwd_dkdv_kernel<D, CAUSAL>, dim3(grid), DkdvCfg<D>::kThreads, DkdvCfg<D>::kSmemBytes, p,
+                       stream);
+}
+
+template <int D, bool CAUSAL>
+int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
+  const BwdParams p = with_q_order(p_in, CAUSAL, D);
+  const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
+  if (!grid) return FA_ERR_UNSUPPORTED;
   auto kern = bwd_dq_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
-  kern<<<dim3((p.N + 127) / 128, p.H, p.B), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(
+  kern<<<dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(
       p, static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.dO));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -1293,9 +1331,12 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
     case 64: return causal ? launch_dkdv_t<64, true>(p, stream) : launch_dkdv_t<64, false>(p, stream);
     case 128: return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
     case 256: {
-      const dim3 grid(2 * ((p.N + 127) / 128), p.Hkv, p.B);  // x: (key tile, head-dim half)
-      return causal ? launch_kernel(bwd_dkdv256_kernel<true>, grid, Dkdv256Cfg<true>::kThreads, Dkdv256Cfg<true>::kSmemBytes, p, stream)
-                    : launch_kernel(bwd_dkdv256_kernel<false>, grid, Dkdv256Cfg<false>::kThreads, Dkdv256Cfg<false>::kSmemBytes, p, stream);
+      const BwdParams q = with_kv_order(p, causal, 256);
+      const unsigned n = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.Hkv);  // (key tile, head-dim half)
+      if (!n) return FA_ERR_UNSUPPORTED;
+      const dim3 grid(n);
+      return causal ? launch_kernel(bwd_dkdv256_kernel<true>, grid, Dkdv256Cfg<true>::kThreads, Dkdv256Cfg<true>::kSmemBytes, q, stream)
+                    : launch_kernel(bwd_dkdv256_kernel<false>, grid, Dkdv256Cfg<false>::kThreads, Dkdv256Cfg<false>::kSmemBytes, q, stream);
     }
     default: return FA_ERR_UNSUPPORTED;
   }
@@ -1306,9 +1347,12 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
     case 64: return causal ? launch_dq_t<64, true>(p, stream) : launch_dq_t<64, false>(p, stream);
     case 128: return causal ? launch_dq_t<128, true>(p, stream) : launch_dq_t<128, false>(p, stream);
     case 256: {
-      const dim3 grid((p.N + 127) / 128, p.H, p.B);
-      return causal ? launch_kernel(bwd_dq256_kernel<true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, p, stream)
-                    : launch_kernel(bwd_dq256_kernel<false>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, p, stream);
+      const BwdParams q = with_q_order(p, causal, 256);
+      const unsigned n = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
+      if (!n) return FA_ERR_UNSUPPORTED;
+      const dim3 grid(n);
+      return causal ? launch_kernel(bwd_dq256_kernel<true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, q, stream)
+                    : launch_kernel(bwd_dq256_kernel<false>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, q, stream);
     }
     default: return FA_ERR_UNSUPPORTED;
   }

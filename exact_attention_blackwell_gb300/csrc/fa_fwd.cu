@@ -44,7 +44,7 @@ namespace {
 __device__ unsigned long long g_trace_fwd[64][16];
 #define FA_TRACE_EV(j, ev)                                                                       \
   do {                                                                                           \
-    if (blockIdx.x == FA_TRACE_CTA && blockIdx.y == 0 && blockIdx.z == 0 && (j) < 64)            \
+    if (blockIdx.x == FA_TRACE_CTA && (j) < 64)                                                 \
       g_trace_fwd[(j)][(ev)] = clock64();                                                        \
   } while (0)
 #else
@@ -102,8 +102,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int group = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // heaviest first
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int n_groups = (p.N + 128 * QT - 1) / (128 * QT);
+  int rank, head;
+  work_order((int)blockIdx.x, n_groups, p.B * p.H, p.sched_chunk, rank, head);
+  const int group = CAUSAL ? n_groups - 1 - rank : rank;  // causal: the longest query rows first
+  const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
   const int n_kv_all = (p.N + 127) / 128;
 
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
 }
 
 template <int D, bool CAUSAL>
-int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
+int launch_fwd_t(const FwdParams &p_in, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16>;
   static bool configured = false;  // per process; attribute is per function
@@ -432,8 +435,14 @@ int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
     configured = true;
   }
   const int rows_per_cta = 128 * C::kQT;
-  dim3 grid((p.N + rows_per_cta - 1) / rows_per_cta, p.H, p.B);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+  const long long n_groups = (p_in.N + rows_per_cta - 1) / rows_per_cta;
+  const long long n_ctas = n_groups * p_in.H * p_in.B;
+  if (n_ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  FwdParams p = p_in;
+  // K and V of one kv head are re-read by every query tile of its query heads
+  const int g = p.H / p.Hkv;
+  p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * D * 2, p.B * p.Hkv) : 1;
+  kern<<<(unsigned)n_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -32,6 +32,7 @@ struct FwdParams {
   unsigned *status;  // device status word: [0] error bits, [1] failing site, [2] rescale count
   int B, H, Hkv, N;
   float scale_log2;  // scale * log2(e)
+  int sched_chunk;   // heads per scheduling chunk (see work_order)
 };
 
 struct BwdParams {
@@ -45,7 +46,38 @@ struct BwdParams {
   int B, H, Hkv, N;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
+  int sched_chunk;   // heads per scheduling chunk (see work_order)
 };
+
+// CTA order of the main kernels.  Each launch is a 1-D grid of n_heads x
+// n_tiles CTAs; the hardware starts them roughly in index order.  Heads are
+// taken in chunks of `chunk`; inside a chunk the tile rank is the slow index,
+// so the chunk's heads run side by side.  Rank 0 is each kernel's heaviest
+// tile under the causal mask, so the short tiles fill the tail of the launch.
+// The chunk is sized so that the tensors every tile of a head re-reads (K and
+// V, or Q and dO) stay in L2 while the chunk runs; chunk = 1 gives plain
+// head-major order with tiles in rank order (used without the causal mask,
+// where all tiles cost the same).
+constexpr size_t kSchedL2Budget = 32ull << 20;
+
+inline int sched_chunk_for(bool causal, size_t reused_bytes_per_head, int n_heads) {
+  if (!causal || n_heads <= 1) return 1;
+  size_t c = kSchedL2Budget / (reused_bytes_per_head ? reused_bytes_per_head : 1);
+  if (c < 1) c = 1;
+  if (c > (size_t)n_heads) c = (size_t)n_heads;
+  return (int)c;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void work_order(int L, int n_tiles, int n_heads, int chunk, int &rank, int &head) {
+  const int per_chunk = chunk * n_tiles;
+  const int c = L / per_chunk;
+  const int r = L - c * per_chunk;
+  const int hc = min(chunk, n_heads - c * chunk);  // the last chunk may be short
+  rank = r / hc;
+  head = c * chunk + (r - rank * hc);
+}
+#endif
 
 // Device status word of the current device (a small static device array).
 unsigned *device_status_ptr();
