@@ -177,8 +177,6 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   p->lse2 = reinterpret_cast<float *>(ws);
   p->delta = reinterpret_cast<const float *>(ws + up((size_t)B * H * Npad * sizeof(float)));
-  p->q = q;
-  p->dO = dO;
   p->status = device_status_ptr();
   if (!p->status) return FA_ERR_CUDA;
   p->B = B;

@@ -41,6 +41,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 #define FA_TRACE_CTA 7
 #endif
 __device__ unsigned long long g_trace[2][64][16];
+// Lifecycle of CTA FA_TRACE_CTA (SM clock), and for every CTA its SM and the
+// global timer at entry and exit; kernel 0 = dK/dV, 1 = dQ (head dim <= 128).
+__device__ unsigned long long g_life[2][16];
+__device__ unsigned long long g_cta[2][65536][3];
+#define FA_LIFE(k, ev)                                      \
+  do {                                                      \
+    if (blockIdx.x == FA_TRACE_CTA) g_life[(k)][(ev)] = clock64(); \
+  } while (0)
+#define FA_CTA_MARK(k, slot)                                                    \
+  do {                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < 65536) {                               \
+      unsigned sm_;                                                             \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                          \
+      g_cta[(k)][blockIdx.x][0] = sm_;                                          \
+      g_cta[(k)][blockIdx.x][(slot)] = global_timer_ns();                       \
+    }                                                                           \
+  } while (0)
 #define FA_TRACE_EV(k, it, ev)                                                                   \
   do {                                                                                           \
     if (blockIdx.x == FA_TRACE_CTA && (it) < 64)                                                \
@@ -49,6 +66,12 @@ __device__ unsigned long long g_trace[2][64][16];
 #else
 #define FA_TRACE_EV(k, it, ev) \
   do {                         \
+  } while (0)
+#define FA_LIFE(k, ev) \
+  do {                 \
+  } while (0)
+#define FA_CTA_MARK(k, slot) \
+  do {                       \
   } while (0)
 #endif
 
@@ -283,6 +306,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
   const WaitCtx wctx{abort_flag, p.status};
+  FA_CTA_MARK(0, 1);
+  if (threadIdx.x == 0) FA_LIFE(0, 0);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -321,6 +346,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) FA_LIFE(0, 1);
 
   if (warp < 8) {
     // ===================================================== P^T and dS^T, one warpgroup per 64 query columns
@@ -334,6 +360,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
     //      drained once every MMA has completed)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    if (threadIdx.x == 0) FA_LIFE(0, 4);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
     if (ok) acc_to_smem<D>(tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK), stage, r, 0, wg == 0 ? 1.0f : p.scale);
@@ -345,6 +372,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, kv0, b);
       bulk_commit();
       bulk_wait_read_all();
+      if (threadIdx.x == 0) FA_LIFE(0, 5);
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
@@ -394,6 +422,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       if (ok) {
         tc_fence_after();
         issue_s(0);
+        if (lane == 0) FA_LIFE(0, 3);
         ok = full_ok(1);
       }
       if (ok) {
@@ -510,6 +539,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  FA_CTA_MARK(0, 2);
+  if (threadIdx.x == 0) FA_LIFE(0, 6);
 }
 
 // Query-row elementwise work of the dQ kernels over all key tiles: one thread
@@ -603,8 +634,7 @@ struct DqCfg {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p, const __nv_bfloat16 *q,
-                                                        const __nv_bfloat16 *dO) {
+__global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -614,6 +644,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
   const WaitCtx wctx{abort_flag, p.status};
+  FA_CTA_MARK(1, 1);
+  if (threadIdx.x == 0) FA_LIFE(1, 0);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -638,6 +670,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     tmem_relinquish();
   }
   if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_do);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_dq);
@@ -646,6 +680,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) FA_LIFE(1, 1);
 
   if (warp < 8) {
     // ===================================================== dS = P (dP - D), one warpgroup per 64 key columns
@@ -654,23 +689,20 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int q_row = q0 + r;
     {
-      // Q (warpgroup 0) or dO (warpgroup 1): this thread's row, bf16 pairs in
-      // memory order, into TMEM as the A operand of the S / dP MMAs.
-      const __nv_bfloat16 *src = wg == 0 ? q : dO;
+      // Q (warpgroup 0) or dO (warpgroup 1): ring fill 0 / 1 (TMA, zero rows
+      // past N); this thread's row, bf16 pairs in memory order, into TMEM as the
+      // A operand of the S / dP MMAs.
       uint32_t row[D / 2];
-      if (q_row < p.N) {
-        const uint4 *g = reinterpret_cast<const uint4 *>(src + (((size_t)b * p.N + q_row) * p.H + h) * D);
+      const bool got = mbar_wait_warp(bar(C::kBarFull0 + wg), 0, wctx, kBSiteQ);
+      const uint8_t *tile = smem + C::kOffRing + wg * C::kTile;
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) {
-          const uint4 x = g[v];
-          row[4 * v] = x.x;
-          row[4 * v + 1] = x.y;
-          row[4 * v + 2] = x.z;
-          row[4 * v + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < D / 2; ++v) row[v] = 0u;
+      for (int v = 0; v < D / 8; ++v) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (got) x = *reinterpret_cast<const uint4 *>(tile + (v >> 3) * 16384 + r * 128 + (((v & 7) ^ (r & 7)) << 4));
+        row[4 * v] = x.x;
+        row[4 * v + 1] = x.y;
+        row[4 * v + 2] = x.z;
+        row[4 * v + 3] = x.w;
       }
       const uint32_t dst = tmem + lane_off + (wg == 0 ? C::kColQ : C::kColDO);
 #pragma unroll
@@ -681,6 +713,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kBarQdo));
+      if (threadIdx.x == 0) FA_LIFE(1, 2);
     }
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
     const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
@@ -688,6 +721,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt);
     // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    if (threadIdx.x == 0) FA_LIFE(1, 4);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffStage;
     if (ok) acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
@@ -697,6 +731,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, q0, b);
       bulk_commit();
       bulk_wait_read_all();
+      if (threadIdx.x == 0) FA_LIFE(1, 5);
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
@@ -714,32 +749,42 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       auto slot_off = [](int fill) { return (uint64_t)(((fill % C::kStages) * C::kTile) >> 4); };
       auto par = [](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T (K_j is fill 2j)
+      // ring fills 0 and 1 held Q and dO; K_j is fill 2 + 2j, V_j fill 3 + 2j
+      auto fk = [](int j) { return 2 + 2 * j; };
+      auto fv = [](int j) { return 3 + 2 * j; };
+      auto issue_s = [&](int j) {  // S_j = Q K_j^T
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(2 * j) + kmaj(kk), id_s, kk > 0);
+            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(fk(j)) + kmaj(kk), id_s, kk > 0);
           tc_commit(bar(C::kBarS));
         }
         __syncwarp();
       };
-      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T (V_j is fill 2j + 1)
+      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(2 * j + 1) + kmaj(kk), id_s,
+            mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj(kk), id_s,
                    kk > 0);
           tc_commit(bar(C::kBarDP));
-          tc_commit(bar(C::kBarEmpty0 + (2 * j + 1) % C::kStages));  // V_j consumed
+          tc_commit(bar(C::kBarEmpty0 + fv(j) % C::kStages));  // V_j consumed
         }
         __syncwarp();
       };
       bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
-      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0), par(0), wctx, kBSiteFull);
+      // Q and dO are in TMEM: ring slots 0 and 1 may take K/V fills
+      if (ok && elect_one()) {
+        mbar_arrive(bar(C::kBarEmpty0 + 0));
+        mbar_arrive(bar(C::kBarEmpty0 + 1));
+      }
+      __syncwarp();
+      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + fk(0) % C::kStages), par(fk(0)), wctx, kBSiteFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        ok = mbar_wait_warp(bar(C::kBarFull0 + 1 % C::kStages), par(1), wctx, kBSiteFull);
+        if (lane == 0) FA_LIFE(1, 3);
+        ok = mbar_wait_warp(bar(C::kBarFull0 + fv(0) % C::kStages), par(fv(0)), wctx, kBSiteFull);
       }
       if (ok) {
         tc_fence_after();
@@ -751,7 +796,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         if (more) {
           ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
           FA_TRACE_EV(1, j, 12);
-          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + (2 * j + 2) % C::kStages), par(2 * j + 2), wctx, kBSiteFull);
+          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + fk(j + 1) % C::kStages), par(fk(j + 1)), wctx, kBSiteFull);
           if (!ok) break;
           FA_TRACE_EV(1, j, 13);
           tc_fence_after();
@@ -765,13 +810,13 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(2 * j) + (uint64_t)(kk * 128),
+            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128),
                    id_dq, (j > 0 || kk > 0));
-          tc_commit(bar(C::kBarEmpty0 + (2 * j) % C::kStages));  // K_j consumed
+          tc_commit(bar(C::kBarEmpty0 + fk(j) % C::kStages));  // K_j consumed
         }
         __syncwarp();
         if (more) {
-          ok = mbar_wait_warp(bar(C::kBarFull0 + (2 * j + 3) % C::kStages), par(2 * j + 3), wctx, kBSiteFull);
+          ok = mbar_wait_warp(bar(C::kBarFull0 + fv(j + 1) % C::kStages), par(fv(j + 1)), wctx, kBSiteFull);
           if (!ok) break;
           tc_fence_after();
           issue_dp(j + 1);
@@ -789,11 +834,20 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       }
     }
   } else {
-    // ===================================================== TMA producer: K_j, V_j alternating through the ring
+    // ===================================================== TMA producer: Q, dO, then K_j, V_j alternating
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();  // K, V are re-read by every query tile
+      const uint64_t once = policy_evict_first();  // this CTA's Q and dO rows are read once
+      // fills 0, 1: Q and dO (fresh slots; the MMA warp releases them once the
+      // elementwise warps have copied them into TMEM)
+      for (int t = 0; t < 2; ++t) {
+        mbar_arrive_expect_tx(bar(C::kBarFull0 + t), C::kTile);
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_4d_hint(sbase + C::kOffRing + t * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
+                           bar(C::kBarFull0 + t), bx * 64, h, q0, b, once);
+      }
       bool ok = true;
-      int fill = 0;
+      int fill = 2;
       for (int j = 0; j < nb && ok; ++j) {
         for (int kv = 0; kv < 2 && ok; ++kv, ++fill) {
           const int s = fill % C::kStages;
@@ -819,6 +873,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  FA_CTA_MARK(1, 2);
+  if (threadIdx.x == 0) FA_LIFE(1, 6);
 }
 
 // ================================================================== head dim 256
@@ -1310,8 +1366,7 @@ int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   auto kern = bwd_dq_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
-  kern<<<dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(
-      p, static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.dO));
+  kern<<<dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -1363,5 +1418,10 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
 #ifdef FA_TRACE
 extern "C" int fa_debug_trace(unsigned long long *host_out) {
   return cudaMemcpyFromSymbol(host_out, fa::g_trace, sizeof(fa::g_trace)) == cudaSuccess ? 0 : -5;
+}
+// life: 2 x 16 SM-clock stamps; ctas: 2 x 65536 x {smid, entry ns, exit ns}
+extern "C" int fa_debug_trace_ctas(unsigned long long *life, unsigned long long *ctas) {
+  if (cudaMemcpyFromSymbol(life, fa::g_life, sizeof(fa::g_life)) != cudaSuccess) return -5;
+  return cudaMemcpyFromSymbol(ctas, fa::g_cta, sizeof(fa::g_cta)) == cudaSuccess ? 0 : -5;
 }
 #endif

@@ -42,6 +42,23 @@ namespace {
 #define FA_TRACE_CTA 7
 #endif
 __device__ unsigned long long g_trace_fwd[64][16];
+// Lifecycle of CTA FA_TRACE_CTA (SM clock), and for every CTA its SM and the
+// global timer at entry and exit.
+__device__ unsigned long long g_life_fwd[16];
+__device__ unsigned long long g_cta_fwd[65536][3];
+#define FA_LIFE(ev)                                                   \
+  do {                                                                \
+    if (blockIdx.x == FA_TRACE_CTA) g_life_fwd[(ev)] = clock64();     \
+  } while (0)
+#define FA_CTA_MARK(slot)                                                       \
+  do {                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < 65536) {                               \
+      unsigned sm_;                                                             \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                          \
+      g_cta_fwd[blockIdx.x][0] = sm_;                                           \
+      g_cta_fwd[blockIdx.x][(slot)] = global_timer_ns();                        \
+    }                                                                           \
+  } while (0)
 #define FA_TRACE_EV(j, ev)                                                                       \
   do {                                                                                           \
     if (blockIdx.x == FA_TRACE_CTA && (j) < 64)                                                 \
@@ -50,6 +67,12 @@ __device__ unsigned long long g_trace_fwd[64][16];
 #else
 #define FA_TRACE_EV(j, ev) \
   do {                     \
+  } while (0)
+#define FA_LIFE(ev) \
+  do {              \
+  } while (0)
+#define FA_CTA_MARK(slot) \
+  do {                    \
   } while (0)
 #endif
 
@@ -99,6 +122,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
   const WaitCtx wctx{abort_flag, p.status};
+  FA_CTA_MARK(1);
+  if (threadIdx.x == 0) FA_LIFE(0);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -144,6 +169,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) FA_LIFE(1);
 
   if (warp < 4 * QT) {
     // ===================================================== softmax warpgroups
@@ -252,6 +278,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
     // ----------------------------------------------------- epilogue
     if (nb[t] > 0) {
       if (ok) ok = mbar_wait_warp(o_bar(t), 0, wctx, kSiteOFull);
+      if (threadIdx.x == 0) FA_LIFE(4);
       tc_fence_after();
       uint8_t *stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is dead once O_t is final
       if (ok) {
@@ -284,6 +311,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
         for (int bx = 0; bx < C::kBoxes; ++bx) tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, q0[t], b);
         bulk_commit();
         bulk_wait_read_all();
+        if (threadIdx.x == 0) FA_LIFE(5);
       }
     }
     if (rescales) atomicAdd(p.status + 2, rescales);
@@ -334,6 +362,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
           tc_commit(empty_bar(slot_of(0)));
         }
         __syncwarp();
+        if (lane == 0) FA_LIFE(3);
       }
       for (int j = 0; j < nb_max && ok; ++j) {
         const int fv = 2 * j + 1, fk = 2 * j + 2;
@@ -422,6 +451,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  FA_CTA_MARK(2);
+  if (threadIdx.x == 0) FA_LIFE(6);
 }
 
 template <int D, bool CAUSAL>
@@ -462,5 +493,10 @@ int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream) {
 #ifdef FA_TRACE
 extern "C" int fa_debug_trace_fwd(unsigned long long *host_out) {
   return cudaMemcpyFromSymbol(host_out, fa::g_trace_fwd, sizeof(fa::g_trace_fwd)) == cudaSuccess ? 0 : -5;
+}
+// life: 16 SM-clock stamps; ctas: 65536 x {smid, entry ns, exit ns}
+extern "C" int fa_debug_trace_ctas_fwd(unsigned long long *life, unsigned long long *ctas) {
+  if (cudaMemcpyFromSymbol(life, fa::g_life_fwd, sizeof(fa::g_life_fwd)) != cudaSuccess) return -5;
+  return cudaMemcpyFromSymbol(ctas, fa::g_cta_fwd, sizeof(fa::g_cta_fwd)) == cudaSuccess ? 0 : -5;
 }
 #endif

@@ -39,7 +39,6 @@ struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
   CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
   CUtensorMap tm_dq;                    // store [B, N, H, d]
-  const void *q, *dO;                   // raw bf16 pointers (rows read directly by the dQ kernel)
   float *lse2;                          // [B, H, Npad] LSE * log2(e) (workspace)
   const float *delta;                   // [B, H, Npad] D = rowsum(dO * O) (workspace)
   unsigned *status;
