@@ -28,6 +28,7 @@ FA_ERR_TIMEOUT = -6
 _P, _I, _F, _LL, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_prepare": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
@@ -89,6 +90,11 @@ def status_string(status: int) -> str:
 def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
     return lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, float(scale),
                         int(bool(causal)), _stream(stream))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale, causal, stream=None) -> int:
+    return lib().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B, max_seqlen, total,
+                               H, Hkv, d, float(scale), int(bool(causal)), _stream(stream))
 
 
 def fa_bwd_workspace_bytes(B, H, Hkv, N, d) -> int:
@@ -155,6 +161,24 @@ def attention_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=
     st = fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream)
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, out=None, lse=None,
+                         stream=None):
+    """Packed batch: q [total,H,d], k/v [total,Hkv,d] bf16 CUDA tensors, cu_seqlens an int32
+    CUDA tensor [B+1] -> (o bf16 [total,H,d], lse fp32 [H,total])."""
+    import torch
+
+    total, H, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, int(max_seqlen), total, H, Hkv, d, scale, causal, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
     return o, lse
 
 

@@ -56,6 +56,15 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale) {
   return FA_OK;
 }
 
+// Varlen arguments: the table must be a 4-byte aligned device array of B + 1
+// entries (its contents are not read on the host); total rows >= 0.
+int check_varlen(const int *cu_seqlens, int total, int H, int d) {
+  if (cu_seqlens == nullptr || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
+  if (total < 0) return FA_ERR_INVALID_ARG;
+  if ((long long)total * H * d >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 }  // namespace
 
 unsigned *device_status_ptr() {
@@ -126,6 +135,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   if (encode_bf16_tile_map(&p.tm_q, q, B, N, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
       encode_bf16_tile_map(&p.tm_v, v, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_o, o, B, N, H, d, 128))
     return FA_ERR_CUDA;
+  p.o = o;
   p.lse = lse;
   p.status = device_status_ptr();
   if (!p.status) return FA_ERR_CUDA;
@@ -133,6 +143,37 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   p.H = H;
   p.Hkv = Hkv;
   p.N = N;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_fwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens, int B,
+                  int max_seqlen, int total, int H, int Hkv, int d, float scale, int causal, void *stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, max_seqlen, d, scale);
+  if (rc != FA_OK) return rc;
+  if ((rc = check_varlen(cu_seqlens, total, H, d)) != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FA_ERR_ALIGNMENT;
+  if ((rc = check_device()) != FA_OK) return rc;
+  if (total == 0) return FA_OK;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  // the packed tensors as one batch of `total` rows
+  if (encode_bf16_tile_map(&p.tm_q, q, 1, total, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, 1, total, Hkv, d, 128) ||
+      encode_bf16_tile_map(&p.tm_v, v, 1, total, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_o, o, 1, total, H, d, 128))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.total = total;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = max_seqlen;
   p.scale_log2 = scale * 1.4426950408889634f;
   return launch_fwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
 }

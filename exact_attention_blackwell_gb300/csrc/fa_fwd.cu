@@ -28,6 +28,8 @@
 // maximum m_ref is only moved (with an O rescale) when a new block's maximum
 // exceeds it by more than kRescaleTau.  The result is exact either way: O and l
 // share the same stale m_ref, and O / l and m_ref + log2 l are what is stored.
+#include <cuda_bf16.h>
+
 #include "exp2_poly.cuh"
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -104,7 +106,7 @@ enum WaitSite : int {
   kSiteSFull = 6, kSiteOFull = 7, kSiteDrain = 8
 };
 
-template <int D, bool CAUSAL, int POLY16>
+template <int D, bool CAUSAL, int POLY16, bool VARLEN>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int QT = C::kQT;
@@ -133,15 +135,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   const int group = CAUSAL ? n_groups - 1 - rank : rank;  // causal: the longest query rows first
   const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
-  const int n_kv_all = (p.N + 127) / 128;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;  // rows of this sequence (queries and keys)
+  const int n_kv_all = (L + 127) / 128;
 
   int q0[QT], nb[QT];
   int nb_max = 0;
 #pragma unroll
   for (int t = 0; t < QT; ++t) {
     q0[t] = (group * QT + t) * 128;
-    if (q0[t] >= p.N) nb[t] = 0;
-    else nb[t] = CAUSAL ? (min(q0[t] + 127, p.N - 1) / 128 + 1) : n_kv_all;
+    if (q0[t] >= L) nb[t] = 0;
+    else nb[t] = CAUSAL ? (min(q0[t] + 127, L - 1) / 128 + 1) : n_kv_all;
     nb_max = max(nb_max, nb[t]);
   }
 
@@ -203,9 +207,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       if (r == 0) FA_TRACE_EV(j, 1 + 4 * t);
 
       const int kv0 = j * 128;
-      const bool need_mask = (kv0 + 128 > p.N) || (CAUSAL && kv0 + 127 > q0[t]);
+      const bool need_mask = (kv0 + 128 > L) || (CAUSAL && kv0 + 127 > q0[t]);
       if (need_mask) {
-        const int lim = CAUSAL ? min(p.N - 1, q_row) - kv0 : p.N - 1 - kv0;  // last visible column
+        const int lim = CAUSAL ? min(L - 1, q_row) - kv0 : L - 1 - kv0;  // last visible column
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = -INFINITY;
@@ -281,8 +285,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       if (threadIdx.x == 0) FA_LIFE(4);
       tc_fence_after();
       uint8_t *stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is dead once O_t is final
+      // A varlen tile that runs past its sequence is written row by row (the
+      // rows after it belong to the next sequence); every other tile goes
+      // through shared memory and one TMA store per 64-column box.
+      const bool direct = VARLEN && q0[t] + 128 > L;
       if (ok) {
         const float inv_l = 1.0f / l_sum;
+        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) +
+                                                ((size_t)(sq.start + q_row) * p.H + h) * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -292,23 +302,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          const int box = c >> 1;
+          if (direct) {
+            if (q_row < L) {
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int chunk = ((c & 1) * 4 + k4) ^ (r & 7);
-            uint4 *dst = reinterpret_cast<uint4 *>(stage + box * 16384 + r * 128 + chunk * 16);
-            *dst = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+              for (int k4 = 0; k4 < 4; ++k4)
+                orow[4 * c + k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+            }
+          } else {
+            const int box = c >> 1;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int chunk = ((c & 1) * 4 + k4) ^ (r & 7);
+              uint4 *dst = reinterpret_cast<uint4 *>(stage + box * 16384 + r * 128 + chunk * 16);
+              *dst = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+            }
           }
         }
-        if (p.lse != nullptr && q_row < p.N)
-          p.lse[((size_t)b * p.H + h) * p.N + q_row] = (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+        if (p.lse != nullptr && q_row < L) {
+          const size_t li = VARLEN ? (size_t)h * p.total + sq.start + q_row : ((size_t)b * p.H + h) * p.N + q_row;
+          p.lse[li] = (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+        }
       }
       fence_proxy_async_smem();
       if (t == 0) named_bar_sync(1, 128);
       else named_bar_sync(2, 128);
-      if (r == 0 && ok) {
+      if (r == 0 && ok && !direct) {
 #pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, q0[t], b);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, sq.start + q0[t], sq.bc);
         bulk_commit();
         bulk_wait_read_all();
         if (threadIdx.x == 0) FA_LIFE(5);
@@ -424,7 +445,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       for (int t = 0; t < QT; ++t)
         if (nb[t] > 0)
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d_hint(q_smem + t * C::kTileBytes + bx * 16384, &p.tm_q, q_bar, bx * 64, h, q0[t], b, once);
+            tma_load_4d_hint(q_smem + t * C::kTileBytes + bx * 16384, &p.tm_q, q_bar, bx * 64, h, sq.start + q0[t],
+                             sq.bc, once);
       bool ok = true;
       int fill = 0;
       for (int j = 0; j < nb_max && ok; ++j) {
@@ -435,7 +457,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
           mbar_arrive_expect_tx(full_bar(s), C::kTileBytes);
           const CUtensorMap *map = kv ? &p.tm_v : &p.tm_k;
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d_hint(ring + s * C::kTileBytes + bx * 16384, map, full_bar(s), bx * 64, kh, j * 128, b, keep);
+            tma_load_4d_hint(ring + s * C::kTileBytes + bx * 16384, map, full_bar(s), bx * 64, kh, sq.start + j * 128,
+                             sq.bc, keep);
         }
       }
       // Every copy issued lands before the CTA exits (normally they already have).
@@ -455,10 +478,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   if (threadIdx.x == 0) FA_LIFE(6);
 }
 
-template <int D, bool CAUSAL>
-int launch_fwd_t(const FwdParams &p_in, cudaStream_t stream) {
+template <int D, bool CAUSAL, bool VARLEN>
+int launch_fwd_v(const FwdParams &p_in, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16, VARLEN>;
   static bool configured = false;  // per process; attribute is per function
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -475,6 +498,11 @@ int launch_fwd_t(const FwdParams &p_in, cudaStream_t stream) {
   p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * D * 2, p.B * p.Hkv) : 1;
   kern<<<(unsigned)n_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL>
+int launch_fwd_t(const FwdParams &p, cudaStream_t stream) {
+  return p.cu_seqlens ? launch_fwd_v<D, CAUSAL, true>(p, stream) : launch_fwd_v<D, CAUSAL, false>(p, stream);
 }
 
 }  // namespace

@@ -33,6 +33,12 @@ struct FwdParams {
   int B, H, Hkv, N;
   float scale_log2;  // scale * log2(e)
   int sched_chunk;   // heads per scheduling chunk (see work_order)
+  // Packed variable-length batch (nullptr: B sequences of N rows each).  With a
+  // table, N is the longest sequence, tensors are [total, Hx, d] (the tensor
+  // maps see them as one batch of `total` rows) and lse is [H, total].
+  const int *cu_seqlens;
+  int total;
+  void *o;  // output rows of partial varlen tiles are written directly
 };
 
 struct BwdParams {
@@ -46,6 +52,16 @@ struct BwdParams {
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   int sched_chunk;   // heads per scheduling chunk (see work_order)
+  const int *cu_seqlens;  // as in FwdParams
+  int total;
+};
+
+// Rows of sequence b: the first one's index in the tensor's row dimension, the
+// length, and the batch coordinate of the tensor maps.  A table entry outside
+// its contract is clamped to [0, N] rows inside [0, total), so it can give
+// wrong numbers but never an out-of-bounds access.
+struct SeqSpan {
+  int start, len, bc;
 };
 
 // CTA order of the main kernels.  Each launch is a 1-D grid of n_heads x
@@ -68,6 +84,14 @@ inline int sched_chunk_for(bool causal, size_t reused_bytes_per_head, int n_head
 }
 
 #ifdef __CUDACC__
+__device__ __forceinline__ SeqSpan seq_span(const int *cu, int b, int N, int total) {
+  if (cu == nullptr) return SeqSpan{0, N, b};
+  int s0 = cu[b], s1 = cu[b + 1];
+  s0 = max(0, min(s0, total));
+  const int len = max(0, min(s1 - s0, min(N, total - s0)));
+  return SeqSpan{s0, len, 0};
+}
+
 __device__ __forceinline__ void work_order(int L, int n_tiles, int n_heads, int chunk, int &rank, int &head) {
   const int per_chunk = chunk * n_tiles;
   const int c = L / per_chunk;

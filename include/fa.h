@@ -64,6 +64,27 @@ typedef enum {
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
 
+/* Forward pass over a packed batch of variable-length sequences.  The pages
+ * only name this variant (FlashAttention-4 paper summary, section 5: varlen
+ * among the attention variants the code base is meant to take up); what it
+ * computes here is the plain reading: sequence b is rows
+ * [cu_seqlens[b], cu_seqlens[b+1]) of every tensor, and each sequence is the
+ * single-sequence problem above on its own rows (queries and keys share the
+ * lengths; the causal mask is taken within the sequence, key j visible from
+ * query i iff j <= i).
+ *   q, o : bf16 [total, H, d];  k, v : bf16 [total, Hkv, d];
+ *   lse  : fp32 [H, total] (natural log) or NULL;
+ *   cu_seqlens : DEVICE int32 [B + 1], cu_seqlens[0] = 0, non-decreasing,
+ *     cu_seqlens[B] = total, every length <= max_seqlen.  The table is read
+ *     only on the device: lengths are clamped to [0, max_seqlen] and rows to
+ *     [0, total), so a table outside this contract gives unspecified values
+ *     but no out-of-bounds access.  Rows of empty sequences are not written.
+ * total = 0 is valid and launches nothing.  Other rules as for fa_fwd
+ * (max_seqlen takes the place of N in the size limits). */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *cu_seqlens, int B, int max_seqlen, int total,
+                  int H, int Hkv, int d, float scale, int causal, void *stream);
+
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row-term
  * arrays [B,H,Npad] (D = rowsum(dO * O) and the log2-scaled LSE), Npad = N
  * rounded up to a multiple of 128, each starting on a 256-byte boundary.

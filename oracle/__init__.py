@@ -123,3 +123,41 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool, qrows=None, kvrows=No
     _load().oracle_bwd_rows(_dp(q), _dp(k), _dp(v), _dp(dO), B, H, Hkv, N, d, float(scale),
                             int(bool(causal)), _ip(qr), nq, _ip(kr), nkv, _dp(dq), _dp(dk), _dp(dv))
     return dq, dk, dv
+
+
+def _seq_bounds(cu_seqlens):
+    cu = np.asarray(cu_seqlens.detach().cpu() if hasattr(cu_seqlens, "detach") else cu_seqlens, dtype=np.int64)
+    assert cu.ndim == 1 and cu.size >= 2 and cu[0] == 0 and (np.diff(cu) >= 0).all()
+    return [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:])]
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, scale: float, causal: bool):
+    """Packed variable-length forward: sequence b is rows [cu[b], cu[b+1]) of
+    q [total, H, d] and k, v [total, Hkv, d], and is the single-sequence
+    problem of :func:`attention_fwd` on those rows (the plain reading of the
+    varlen variant the FlashAttention-4 paper summary names in section 5).
+    Returns (O [total, H, d], LSE [H, total]) in fp64; rows of no sequence stay 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, H, d = q.shape
+    o = np.zeros((total, H, d), np.float64)
+    lse = np.zeros((H, total), np.float64)
+    for a, b in _seq_bounds(cu_seqlens):
+        if b == a:
+            continue
+        ob, lb = attention_fwd(q[None, a:b], k[None, a:b], v[None, a:b], scale, causal)
+        o[a:b] = ob[0]
+        lse[:, a:b] = lb[0]
+    return o, lse
+
+
+def attention_bwd_varlen(q, k, v, dO, cu_seqlens, scale: float, causal: bool):
+    """Packed variable-length backward, per sequence as in :func:`attention_fwd_varlen`.
+    Returns (dQ [total, H, d], dK, dV [total, Hkv, d]) in fp64."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for a, b in _seq_bounds(cu_seqlens):
+        if b == a:
+            continue
+        g = attention_bwd(q[None, a:b], k[None, a:b], v[None, a:b], dO[None, a:b], scale, causal)
+        dq[a:b], dk[a:b], dv[a:b] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv

@@ -118,3 +118,22 @@ def test_exp2_rejects_bad_arguments(lib):
     assert fa.fa_exp2_poly(A, A, -1, 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_exp2_poly(A + 1, A, 5, 0) == fa.FA_ERR_ALIGNMENT
     assert fa.fa_exp2_poly(None, None, 0, 0) == fa.FA_OK
+
+
+def test_fwd_varlen_rejects_bad_arguments(lib):
+    # q, k, v, o, lse, cu, B, max_seqlen, total, H, Hkv, d, scale, causal, stream
+    ok = dict(q=A, k=A, v=A, o=A, lse=A, cu=A, B=2, L=300, total=400, H=4, Hkv=2, d=128, scale=0.1)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["B"], a["L"], a["total"], a["H"],
+                                a["Hkv"], a["d"], a["scale"], 0, 0)
+
+    assert call(cu=None) == fa.FA_ERR_INVALID_ARG
+    assert call(cu=A + 2) == fa.FA_ERR_INVALID_ARG  # the table must be 4-byte aligned
+    assert call(total=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(L=0) == fa.FA_ERR_INVALID_ARG
+    assert call(B=0) == fa.FA_ERR_INVALID_ARG
+    assert call(H=3) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(q=A + 8) == fa.FA_ERR_ALIGNMENT

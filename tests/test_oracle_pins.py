@@ -236,3 +236,54 @@ def test_row_selection_matches_full(oracle_mod, causal):
     np.testing.assert_array_equal(dqs, dq[:, rows])
     np.testing.assert_array_equal(dks, dk[:, rows[::-1]])
     np.testing.assert_array_equal(dvs, dv[:, rows[::-1]])
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+def test_varlen_single_row_sequences_are_closed_form(oracle_mod):
+    # every sequence has one row: softmax over one key, so O = v and LSE = scale q.k
+    total, H, Hkv, d, scale = 5, 4, 2, 8, 0.3
+    q, k, v = rnd((total, H, d), 1), rnd((total, Hkv, d), 2), rnd((total, Hkv, d), 3)
+    cu = np.arange(total + 1)
+    for causal in (False, True):
+        o, lse = oracle_mod.attention_fwd_varlen(q, k, v, cu, scale, causal)
+        kv = np.repeat(np.arange(Hkv), H // Hkv)
+        np.testing.assert_allclose(o, v[:, kv, :], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse, scale * np.einsum("thd,thd->ht", q, k[:, kv, :]), rtol=1e-14, atol=1e-14)
+
+
+def test_varlen_equal_lengths_match_the_batched_problem(oracle_mod):
+    B, N, H, Hkv, d = 3, 7, 4, 2, 8
+    q, k, v = qkv(B, N, H, Hkv, d, 40)
+    dO = rnd((B, N, H, d), 44)
+    cu = np.arange(B + 1) * N
+    for causal in (False, True):
+        o, lse = oracle_mod.attention_fwd(q, k, v, 0.4, causal)
+        ov, lv = oracle_mod.attention_fwd_varlen(q.reshape(B * N, H, d), k.reshape(B * N, Hkv, d),
+                                                 v.reshape(B * N, Hkv, d), cu, 0.4, causal)
+        np.testing.assert_array_equal(ov, o.reshape(B * N, H, d))
+        np.testing.assert_array_equal(lv, lse.transpose(1, 0, 2).reshape(H, B * N))
+        g = oracle_mod.attention_bwd(q, k, v, dO, 0.4, causal)
+        gv = oracle_mod.attention_bwd_varlen(q.reshape(B * N, H, d), k.reshape(B * N, Hkv, d),
+                                             v.reshape(B * N, Hkv, d), dO.reshape(B * N, H, d), cu, 0.4, causal)
+        for a, b in zip(gv, g):
+            np.testing.assert_array_equal(a, b.reshape(a.shape))
+
+
+def test_varlen_sequences_do_not_see_each_other(oracle_mod):
+    # changing sequence 1 leaves sequence 0's outputs and gradients unchanged
+    H, Hkv, d = 2, 1, 8
+    cu = np.array([0, 5, 9])
+    q, k, v = rnd((9, H, d), 50), rnd((9, Hkv, d), 51), rnd((9, Hkv, d), 52)
+    dO = rnd((9, H, d), 53)
+    o1, l1 = oracle_mod.attention_fwd_varlen(q, k, v, cu, 0.5, False)
+    g1 = oracle_mod.attention_bwd_varlen(q, k, v, dO, cu, 0.5, False)
+    k2, v2 = k.copy(), v.copy()
+    k2[5:] += 3.0
+    v2[5:] -= 2.0
+    o2, l2 = oracle_mod.attention_fwd_varlen(q, k2, v2, cu, 0.5, False)
+    g2 = oracle_mod.attention_bwd_varlen(q, k2, v2, dO, cu, 0.5, False)
+    np.testing.assert_array_equal(o1[:5], o2[:5])
+    np.testing.assert_array_equal(l1[:, :5], l2[:, :5])
+    for a, b in zip(g1, g2):
+        np.testing.assert_array_equal(a[:5], b[:5])
+    assert not np.allclose(o1[5:], o2[5:])
