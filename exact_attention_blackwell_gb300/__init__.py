@@ -31,6 +31,7 @@ SIGNATURES = {
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_prepare": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -108,6 +109,13 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, work
                         _stream(stream))
 
 
+def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale, causal,
+                  workspace, workspace_bytes, stream=None) -> int:
+    return lib().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(cu_seqlens), B, max_seqlen, total, H, Hkv, d, float(scale), int(bool(causal)),
+                               _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def fa_bwd_prepare(o, lse, dO, B, H, Hkv, N, d, workspace, workspace_bytes, stream=None) -> int:
     return lib().fa_bwd_prepare(_ptr(o), _ptr(lse), _ptr(dO), B, H, Hkv, N, d, _ptr(workspace),
                                 int(workspace_bytes), _stream(stream))
@@ -180,6 +188,24 @@ def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=Fal
     if st != FA_OK:
         raise FaError(st, "fa_fwd_varlen")
     return o, lse
+
+
+def attention_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen, scale=None, causal=False, stream=None):
+    """Packed batch backward (layouts of :func:`attention_fwd_varlen`) -> (dq, dk, dv) bf16."""
+    import torch
+
+    total, H, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa_bwd_workspace_bytes(B, H, Hkv, int(max_seqlen), d)
+    workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    st = fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, B, int(max_seqlen), total, H, Hkv, d, scale,
+                       causal, workspace, nbytes, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def attention_bwd(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None):

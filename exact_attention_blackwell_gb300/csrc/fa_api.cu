@@ -192,11 +192,14 @@ namespace {
 
 // Validation and parameter set-up shared by fa_bwd and its three stages.
 // Pointers passed as nullptr are not needed by the stage and are not checked.
+// With a varlen table (cu != nullptr) N is the longest sequence and the tensors
+// are packed [total, Hx, d]; the row-term workspace keeps its [B, H, Npad] layout.
 int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const void *dO, const void *dq,
               const void *dk, const void *dv, int B, int H, int Hkv, int N, int d, float scale, void *workspace,
-              size_t workspace_bytes) {
+              size_t workspace_bytes, const int *cu = nullptr, int total = 0) {
   int rc = check_common(B, H, Hkv, N, d, scale);
   if (rc != FA_OK) return rc;
+  if (cu && (rc = check_varlen(cu, total, H, d)) != FA_OK) return rc;
   for (const void *x : {q, k, v, dO, dq, dk, dv})
     if (x && !aligned16(x)) return FA_ERR_ALIGNMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
@@ -204,15 +207,22 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
     return FA_ERR_WORKSPACE;
   if ((rc = check_device()) != FA_OK) return rc;
   std::memset(p, 0, sizeof(*p));
-  // tensor maps of the tensors this stage touches (nullptr: not used by it)
-  if ((q && encode_bf16_tile_map(&p->tm_q, q, B, N, H, d, 128)) ||
-      (k && encode_bf16_tile_map(&p->tm_k, k, B, N, Hkv, d, 128)) ||
-      (v && encode_bf16_tile_map(&p->tm_v, v, B, N, Hkv, d, 128)) ||
-      (dO && encode_bf16_tile_map(&p->tm_do, dO, B, N, H, d, 128)) ||
-      (dq && encode_bf16_tile_map(&p->tm_dq, dq, B, N, H, d, 128)) ||
-      (dk && encode_bf16_tile_map(&p->tm_dk, dk, B, N, Hkv, d, 128)) ||
-      (dv && encode_bf16_tile_map(&p->tm_dv, dv, B, N, Hkv, d, 128)))
+  // tensor maps of the tensors this stage touches (nullptr: not used by it);
+  // packed varlen tensors are one batch of `total` rows
+  const int mb = cu ? 1 : B, mn = cu ? total : N;
+  if ((q && encode_bf16_tile_map(&p->tm_q, q, mb, mn, H, d, 128)) ||
+      (k && encode_bf16_tile_map(&p->tm_k, k, mb, mn, Hkv, d, 128)) ||
+      (v && encode_bf16_tile_map(&p->tm_v, v, mb, mn, Hkv, d, 128)) ||
+      (dO && encode_bf16_tile_map(&p->tm_do, dO, mb, mn, H, d, 128)) ||
+      (dq && encode_bf16_tile_map(&p->tm_dq, dq, mb, mn, H, d, 128)) ||
+      (dk && encode_bf16_tile_map(&p->tm_dk, dk, mb, mn, Hkv, d, 128)) ||
+      (dv && encode_bf16_tile_map(&p->tm_dv, dv, mb, mn, Hkv, d, 128)))
     return FA_ERR_CUDA;
+  p->cu_seqlens = cu;
+  p->total = total;
+  p->dq = const_cast<void *>(dq);
+  p->dk = const_cast<void *>(dk);
+  p->dv = const_cast<void *>(dv);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t Npad = ((size_t)N + 127) / 128 * 128;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -276,6 +286,23 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if ((rc = setup_bwd(&p, q, k, v, dO, dq, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes)) != FA_OK)
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
+  if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_dq(p, d, causal != 0, s);
+}
+
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                  void *dq, void *dk, void *dv, const int *cu_seqlens, int B, int max_seqlen, int total, int H,
+                  int Hkv, int d, float scale, int causal, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
+  if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+  BwdParams p;
+  int rc = setup_bwd(&p, q, k, v, dO, dq, dk, dv, B, H, Hkv, max_seqlen, d, scale, workspace, workspace_bytes,
+                     cu_seqlens, total);
+  if (rc != FA_OK) return rc;
+  if (total == 0) return FA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
   if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
   return launch_bwd_dq(p, d, causal != 0, s);

@@ -82,12 +82,14 @@ template <> struct BfVec<4> { using T = uint2; };
 template <> struct BfVec<8> { using T = uint4; };
 
 // One warp per row (b, n, h) of the padded range n < Npad; lane l holds
-// elements [l E, l E + E) of the row.
+// elements [l E, l E + E) of the row.  With a varlen table (cu != nullptr) the
+// rows of sequence b are packed at its offset and lse is [H, total].
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
-                                                      float *__restrict__ delta, int B, int H, int N, int Npad) {
+                                                      float *__restrict__ delta, int B, int H, int N, int Npad,
+                                                      const int *__restrict__ cu, int total) {
   constexpr int E = D / 32;
   using V = typename BfVec<E>::T;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -98,14 +100,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
   const int n = (int)(bn % Npad);
   const int b = (int)(bn / Npad);
   const size_t rw = ((size_t)b * H + h) * Npad + n;
-  if (n >= N) {
+  const SeqSpan sq = seq_span(cu, b, N, total);
+  if (n >= sq.len) {
     if (lane == 0) {
       lse2[rw] = INFINITY;  // padded query rows: P = 2^(s - inf) = 0
       delta[rw] = 0.f;
     }
     return;
   }
-  const size_t off = (((size_t)b * N + n) * H + h) * D + lane * E;
+  const size_t grow = cu ? (size_t)sq.start + n : (size_t)b * N + n;  // row in the [rows, H, D] tensors
+  const size_t off = (grow * H + h) * D + lane * E;
   const V va = *reinterpret_cast<const V *>(o + off);
   const V vg = *reinterpret_cast<const V *>(dO + off);
   const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    lse2[rw] = lse[((size_t)b * H + h) * N + n] * kLog2e;
+    lse2[rw] = lse[cu ? (size_t)h * total + sq.start + n : ((size_t)b * H + h) * N + n] * kLog2e;
     delta[rw] = acc;
   }
 }
@@ -154,6 +158,27 @@ __device__ __forceinline__ void acc_to_smem(uint32_t tm_row, uint8_t *stage, int
   }
 }
 
+// The same epilogue for one row straight to global memory (bf16 row `dst`,
+// columns [c0, c0 + NCOLS)): used for the rows of a varlen tile that belong to
+// its sequence when the tile runs past the sequence's end.
+template <int NCOLS>
+__device__ __forceinline__ void acc_to_global(uint32_t tm_row, __nv_bfloat16 *dst, int c0, float mul, bool write) {
+#pragma unroll
+  for (int c = 0; c < NCOLS / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tm_row + c0 + 32 * c, v);
+    tmem_wait_ld(v);
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
+    if (write) {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0 + 32 * c);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) d4[k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+    }
+  }
+}
+
 enum BwdSite : int {
   kBSiteKV = 11, kBSiteFull = 12, kBSiteEmpty = 13, kBSiteS = 14, kBSiteDP = 15, kBSiteP = 16, kBSiteDS = 17,
   kBSiteDSFree = 18, kBSiteFinal = 19, kBSiteDrain = 20, kBSiteAlign = 21, kBSiteQ = 22
@@ -176,7 +201,7 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
 template <class C, bool CAUSAL>
 __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *smem, uint32_t bar0, uint32_t tmem,
                                           const WaitCtx &wctx, int warp, int n_iter, int i_start, int per_head,
-                                          int jt, int kv0) {
+                                          int jt, int kv0, int L) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
   const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
   const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
@@ -185,7 +210,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
   const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first 32
   const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
   const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
-  const bool row_valid = kv0 + r < p.N;
+  const bool row_valid = kv0 + r < L;  // key rows past the sequence: P = 0
   bool ok = true;
   for (int it = 0; it < n_iter && ok; ++it) {
     const int rs = it % C::kRowStages;
@@ -295,7 +320,7 @@ struct DkdvCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = DkdvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -317,12 +342,15 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   const int jt = rank;  // key/value tile; causal: tile 0 sees the most query tiles
   const int kh = head % p.Hkv, b = head / p.Hkv;
   const int g = p.H / p.Hkv;
-  const int n_q = (p.N + 127) / 128;
-  const int Npad = n_q * 128;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;  // rows of this sequence
+  const int Npad = (p.N + 127) / 128 * 128;  // row-term arrays are [B, H, Npad]
+  const int kv0 = jt * 128;
+  if (VARLEN && kv0 >= L) return;  // the tile lies past its sequence: no rows to produce
+  const int n_q = (L + 127) / 128;
   const int i_start = CAUSAL ? jt : 0;
   const int per_head = n_q - i_start;
   const int n_iter = g * per_head;  // (head, query tile) pairs, head-major
-  const int kv0 = jt * 128;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
@@ -356,20 +384,29 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0);
+    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0, L);
     // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
     //      drained once every MMA has completed)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     if (threadIdx.x == 0) FA_LIFE(0, 4);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
-    if (ok) acc_to_smem<D>(tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK), stage, r, 0, wg == 0 ? 1.0f : p.scale);
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
+    const bool direct = VARLEN && kv0 + 128 > L;  // the next sequence's rows follow: write row by row
+    if (ok && direct) {
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
+      acc_to_global<D>(acc_tm, out + ((size_t)(sq.start + kv0 + r) * p.Hkv + kh) * D, 0, mul, kv0 + r < L);
+    } else if (ok) {
+      acc_to_smem<D>(acc_tm, stage, r, 0, mul);
+    }
     fence_proxy_async_smem();
     if (wg == 0) named_bar_sync(1, 128);
     else named_bar_sync(2, 128);
-    if (r == 0 && ok) {
+    if (r == 0 && ok && !direct) {
       const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
-      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, kv0, b);
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, sq.start + kv0, sq.bc);
       bulk_commit();
       bulk_wait_read_all();
       if (threadIdx.x == 0) FA_LIFE(0, 5);
@@ -490,8 +527,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       const uint64_t keep = policy_evict_last();  // Q, dO, LSE2, D are re-read by every key tile
       mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTile);
       for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, kv0, b);
-        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, kv0, b);
+        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
+        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
       }
       bool ok = true;
       int fill = 0, rows_issued = 0;
@@ -506,7 +543,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
           mbar_arrive_expect_tx(fb, C::kTile);
           const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
           for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, i * 128, b, keep);
+            tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, sq.start + i * 128, sq.bc,
+                             keep);
         }
         if (!ok) break;
         // LSE2 / D rows of iteration it, into row stage it % kRowStages once the
@@ -549,7 +587,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
 //   dS = P (dP - D)             -> TMEM over dP (bf16, dQ's A operand)
 template <class C, bool CAUSAL>
 __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint32_t tmem, const WaitCtx &wctx,
-                                        int warp, int nb, int q_row, float lse2, float dlt) {
+                                        int warp, int nb, int q_row, float lse2, float dlt, int L) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
   const int wg = warp >> 2;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -570,7 +608,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
     tc_fence_before();
     mbar_arrive(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
     const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
-    const int lim = (CAUSAL ? min(q_row, p.N - 1) : p.N - 1) - kvc0;  // last visible column offset
+    const int lim = (CAUSAL ? min(q_row, L - 1) : L - 1) - kvc0;  // last visible column offset
     float pe[64];
 #pragma unroll
     for (int c = 0; c < 64; c += 2) {
@@ -633,7 +671,7 @@ struct DqCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -655,9 +693,12 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   const int it_q = CAUSAL ? n_q - 1 - rank : rank;  // causal: the longest query rows first
   const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
-  const int Npad = n_q * 128;
+  const int Npad = n_q * 128;  // row-term arrays are [B, H, Npad]
   const int q0 = it_q * 128;
-  const int nb = CAUSAL ? it_q + 1 : n_q;  // key tiles this query tile sees
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;  // rows of this sequence
+  if (VARLEN && q0 >= L) return;  // the tile lies past its sequence: no rows to produce
+  const int nb = CAUSAL ? it_q + 1 : (L + 127) / 128;  // key tiles this query tile sees
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
@@ -718,17 +759,24 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
     const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
     const float dlt = p.delta[rw];
-    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt);
+    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt, L);
     // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     if (threadIdx.x == 0) FA_LIFE(1, 4);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffStage;
-    if (ok) acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
+    const bool direct = VARLEN && q0 + 128 > L;  // the next sequence's rows follow: write row by row
+    if (ok && direct)
+      acc_to_global<D / 2>(tmem + lane_off + C::kColDQ,
+                           static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)(sq.start + q_row) * p.H + h) * D, wg * (D / 2),
+                           p.scale, q_row < L);
+    else if (ok)
+      acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
     fence_proxy_async_smem();
     named_bar_sync(1, 256);
-    if (threadIdx.x == 0 && ok) {
-      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, q0, b);
+    if (threadIdx.x == 0 && ok && !direct) {
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
       bulk_commit();
       bulk_wait_read_all();
       if (threadIdx.x == 0) FA_LIFE(1, 5);
@@ -844,7 +892,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(bar(C::kBarFull0 + t), C::kTile);
         for (int bx = 0; bx < D / 64; ++bx)
           tma_load_4d_hint(sbase + C::kOffRing + t * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
-                           bar(C::kBarFull0 + t), bx * 64, h, q0, b, once);
+                           bar(C::kBarFull0 + t), bx * 64, h, sq.start + q0, sq.bc, once);
       }
       bool ok = true;
       int fill = 2;
@@ -857,7 +905,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
           const CUtensorMap *map = kv ? &p.tm_v : &p.tm_k;
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d_hint(sbase + C::kOffRing + s * C::kTile + bx * 16384, map, bar(C::kBarFull0 + s), bx * 64, kh,
-                             j * 128, b, keep);
+                             sq.start + j * 128, sq.bc, keep);
         }
       }
       const uint64_t t0 = global_timer_ns();
@@ -910,7 +958,7 @@ struct Dkdv256Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_constant__ BwdParams p) {
   using C = Dkdv256Cfg<CAUSAL>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -930,12 +978,15 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
   const int e = rank & 1;    // half of the head dim this CTA produces
   const int kh = head % p.Hkv, b = head / p.Hkv;
   const int g = p.H / p.Hkv;
-  const int n_q = (p.N + 127) / 128;
-  const int Npad = n_q * 128;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;                      // rows of this sequence
+  const int Npad = (p.N + 127) / 128 * 128;  // row-term arrays are [B, H, Npad]
+  const int kv0 = jt * 128;
+  if (VARLEN && kv0 >= L) return;  // the tile lies past its sequence: no rows to produce
+  const int n_q = (L + 127) / 128;
   const int i_start = CAUSAL ? jt : 0;
   const int per_head = n_q - i_start;
   const int n_iter = g * per_head;
-  const int kv0 = jt * 128;
   // per iteration four fills: Q half (1-e), Q half e, dO half (1-e), dO half e
   auto fill_of = [&](int it, bool is_do, int half) { return 4 * it + (is_do ? 2 : 0) + (half == e ? 1 : 0); };
   auto slot_of = [](int fill) { return fill % C::kSlots; };
@@ -961,18 +1012,28 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0);
+    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0, L);
     // ---- epilogue: warpgroup 0 stores dV[:, half e], warpgroup 1 dK[:, half e] * scale (ring slots 0, 1)
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffRing + wg * C::kHalf;
-    if (ok) acc_to_smem<128>(tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK), stage, r, 0, wg == 0 ? 1.0f : p.scale);
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
+    const bool direct = VARLEN && kv0 + 128 > L;  // the next sequence's rows follow: write row by row
+    if (ok && direct) {
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
+      acc_to_global<128>(acc_tm, out + ((size_t)(sq.start + kv0 + r) * p.Hkv + kh) * 256 + 128 * e, 0, mul,
+                         kv0 + r < L);
+    } else if (ok) {
+      acc_to_smem<128>(acc_tm, stage, r, 0, mul);
+    }
     fence_proxy_async_smem();
     if (wg == 0) named_bar_sync(1, 128);
     else named_bar_sync(2, 128);
-    if (r == 0 && ok) {
+    if (r == 0 && ok && !direct) {
       const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
-      for (int bx = 0; bx < 2; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, 128 * e + bx * 64, kh, kv0, b);
+      for (int bx = 0; bx < 2; ++bx)
+        tma_store_4d(map, smem_u32(stage) + bx * 16384, 128 * e + bx * 64, kh, sq.start + kv0, sq.bc);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -1065,8 +1126,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
       const uint64_t keep = policy_evict_last();
       mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTile);
       for (int bx = 0; bx < 4; ++bx) {
-        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, kv0, b);
-        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, kv0, b);
+        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
+        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
       }
       bool ok = true;
       int fill = 0, rows_issued = 0;
@@ -1082,7 +1143,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
           mbar_arrive_expect_tx(fb, C::kHalf);
           for (int bx = 0; bx < 2; ++bx)
             tma_load_4d_hint(sbase + C::kOffRing + s * C::kHalf + bx * 16384, t < 2 ? &p.tm_q : &p.tm_do, fb,
-                             128 * half + bx * 64, hh, i * 128, b, keep);
+                             128 * half + bx * 64, hh, sq.start + i * 128, sq.bc, keep);
         }
         if (!ok) break;
         const int rs = it % C::kRowStages;
@@ -1133,7 +1194,7 @@ struct Dq256Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant__ BwdParams p) {
   using C = Dq256Cfg;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1153,9 +1214,12 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
   const int it_q = CAUSAL ? n_q - 1 - rank : rank;
   const int h = head % p.H, b = head / p.H;
   const int kh = h / (p.H / p.Hkv);
-  const int Npad = n_q * 128;
+  const int Npad = n_q * 128;  // row-term arrays are [B, H, Npad]
   const int q0 = it_q * 128;
-  const int nb = CAUSAL ? it_q + 1 : n_q;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;  // rows of this sequence
+  if (VARLEN && q0 >= L) return;  // the tile lies past its sequence: no rows to produce
+  const int nb = CAUSAL ? it_q + 1 : (L + 127) / 128;
   // per key tile four fills: V half 0, V half 1, K half 0, K half 1
   auto fill_of = [](int j, bool is_k, int half) { return 4 * j + (is_k ? 2 : 0) + half; };
   auto slot_of = [](int fill) { return fill % C::kSlots; };
@@ -1182,16 +1246,23 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
     const float lse2 = p.lse2[rw];
     const float dlt = p.delta[rw];
-    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt);
+    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt, L);
     // ---- epilogue: dQ * scale -> bf16 -> shared (the Q tile, free once every S MMA is done) -> TMA store
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     tc_fence_after();
     uint8_t *stage = smem + C::kOffQ;
-    if (ok) acc_to_smem<128>(tmem + lane_off + C::kColDQ, stage, r, wg * 128, p.scale);
+    const bool direct = VARLEN && q0 + 128 > L;  // the next sequence's rows follow: write row by row
+    if (ok && direct)
+      acc_to_global<128>(tmem + lane_off + C::kColDQ,
+                         static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)(sq.start + q_row) * p.H + h) * 256, wg * 128,
+                         p.scale, q_row < L);
+    else if (ok)
+      acc_to_smem<128>(tmem + lane_off + C::kColDQ, stage, r, wg * 128, p.scale);
     fence_proxy_async_smem();
     named_bar_sync(1, 256);
-    if (threadIdx.x == 0 && ok) {
-      for (int bx = 0; bx < 4; ++bx) tma_store_4d(&p.tm_dq, sbase + C::kOffQ + bx * 16384, bx * 64, h, q0, b);
+    if (threadIdx.x == 0 && ok && !direct) {
+      for (int bx = 0; bx < 4; ++bx)
+        tma_store_4d(&p.tm_dq, sbase + C::kOffQ + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -1274,8 +1345,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
       const uint64_t once = policy_evict_first();
       mbar_arrive_expect_tx(bar(C::kBarQdo), 2 * C::kTile);
       for (int bx = 0; bx < 4; ++bx) {
-        tma_load_4d_hint(sbase + C::kOffQ + bx * 16384, &p.tm_q, bar(C::kBarQdo), bx * 64, h, q0, b, once);
-        tma_load_4d_hint(sbase + C::kOffDO + bx * 16384, &p.tm_do, bar(C::kBarQdo), bx * 64, h, q0, b, once);
+        tma_load_4d_hint(sbase + C::kOffQ + bx * 16384, &p.tm_q, bar(C::kBarQdo), bx * 64, h, sq.start + q0, sq.bc,
+                         once);
+        tma_load_4d_hint(sbase + C::kOffDO + bx * 16384, &p.tm_do, bar(C::kBarQdo), bx * 64, h, sq.start + q0, sq.bc,
+                         once);
       }
       bool ok = true;
       int fill = 0;
@@ -1288,7 +1361,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
           mbar_arrive_expect_tx(fb, C::kHalf);
           for (int bx = 0; bx < 2; ++bx)
             tma_load_4d_hint(sbase + C::kOffRing + s * C::kHalf + bx * 16384, t < 2 ? &p.tm_v : &p.tm_k, fb,
-                             128 * (t & 1) + bx * 64, kh, j * 128, b, keep);
+                             128 * (t & 1) + bx * 64, kh, sq.start + j * 128, sq.bc, keep);
         }
       }
       const uint64_t t0 = global_timer_ns();
@@ -1322,7 +1395,7 @@ int launch_pre_t(const BwdParams &p, const void *o, const void *dO, const float 
   const long long rows = (long long)p.B * Npad * p.H;
   bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, p.lse2,
-      const_cast<float *>(p.delta), p.B, p.H, p.N, Npad);
+      const_cast<float *>(p.delta), p.B, p.H, p.N, Npad, p.cu_seqlens, p.total);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -1354,8 +1427,11 @@ int launch_dkdv_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_kv_order(p_in, CAUSAL, D);
   const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.Hkv);
   if (!grid) return FA_ERR_UNSUPPORTED;
-  return launch_kernel(bwd_dkdv_kernel<D, CAUSAL>, dim3(grid), DkdvCfg<D>::kThreads, DkdvCfg<D>::kSmemBytes, p,
-                       stream);
+  return p.cu_seqlens
+             ? launch_kernel(bwd_dkdv_kernel<D, CAUSAL, true>, dim3(grid), DkdvCfg<D>::kThreads, DkdvCfg<D>::kSmemBytes,
+                             p, stream)
+             : launch_kernel(bwd_dkdv_kernel<D, CAUSAL, false>, dim3(grid), DkdvCfg<D>::kThreads,
+                             DkdvCfg<D>::kSmemBytes, p, stream);
 }
 
 template <int D, bool CAUSAL>
@@ -1363,11 +1439,11 @@ int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_q_order(p_in, CAUSAL, D);
   const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
   if (!grid) return FA_ERR_UNSUPPORTED;
-  auto kern = bwd_dq_kernel<D, CAUSAL>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes) != cudaSuccess)
-    return FA_ERR_CUDA;
-  kern<<<dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return p.cu_seqlens
+             ? launch_kernel(bwd_dq_kernel<D, CAUSAL, true>, dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, p,
+                             stream)
+             : launch_kernel(bwd_dq_kernel<D, CAUSAL, false>, dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, p,
+                             stream);
 }
 
 }  // namespace
@@ -1390,8 +1466,15 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
       const unsigned n = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.Hkv);  // (key tile, head-dim half)
       if (!n) return FA_ERR_UNSUPPORTED;
       const dim3 grid(n);
-      return causal ? launch_kernel(bwd_dkdv256_kernel<true>, grid, Dkdv256Cfg<true>::kThreads, Dkdv256Cfg<true>::kSmemBytes, q, stream)
-                    : launch_kernel(bwd_dkdv256_kernel<false>, grid, Dkdv256Cfg<false>::kThreads, Dkdv256Cfg<false>::kSmemBytes, q, stream);
+      if (causal)
+        return q.cu_seqlens ? launch_kernel(bwd_dkdv256_kernel<true, true>, grid, Dkdv256Cfg<true>::kThreads,
+                                            Dkdv256Cfg<true>::kSmemBytes, q, stream)
+                            : launch_kernel(bwd_dkdv256_kernel<true, false>, grid, Dkdv256Cfg<true>::kThreads,
+                                            Dkdv256Cfg<true>::kSmemBytes, q, stream);
+      return q.cu_seqlens ? launch_kernel(bwd_dkdv256_kernel<false, true>, grid, Dkdv256Cfg<false>::kThreads,
+                                          Dkdv256Cfg<false>::kSmemBytes, q, stream)
+                          : launch_kernel(bwd_dkdv256_kernel<false, false>, grid, Dkdv256Cfg<false>::kThreads,
+                                          Dkdv256Cfg<false>::kSmemBytes, q, stream);
     }
     default: return FA_ERR_UNSUPPORTED;
   }
@@ -1406,8 +1489,15 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
       const unsigned n = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
       if (!n) return FA_ERR_UNSUPPORTED;
       const dim3 grid(n);
-      return causal ? launch_kernel(bwd_dq256_kernel<true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, q, stream)
-                    : launch_kernel(bwd_dq256_kernel<false>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes, q, stream);
+      if (causal)
+        return q.cu_seqlens ? launch_kernel(bwd_dq256_kernel<true, true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes,
+                                            q, stream)
+                            : launch_kernel(bwd_dq256_kernel<true, false>, grid, Dq256Cfg::kThreads,
+                                            Dq256Cfg::kSmemBytes, q, stream);
+      return q.cu_seqlens ? launch_kernel(bwd_dq256_kernel<false, true>, grid, Dq256Cfg::kThreads,
+                                          Dq256Cfg::kSmemBytes, q, stream)
+                          : launch_kernel(bwd_dq256_kernel<false, false>, grid, Dq256Cfg::kThreads,
+                                          Dq256Cfg::kSmemBytes, q, stream);
     }
     default: return FA_ERR_UNSUPPORTED;
   }

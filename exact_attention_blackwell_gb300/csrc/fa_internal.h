@@ -54,6 +54,7 @@ struct BwdParams {
   int sched_chunk;   // heads per scheduling chunk (see work_order)
   const int *cu_seqlens;  // as in FwdParams
   int total;
+  void *dq, *dk, *dv;  // rows of partial varlen tiles are written directly
 };
 
 // Rows of sequence b: the first one's index in the tensor's row dimension, the

@@ -101,6 +101,17 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            int B, int H, int Hkv, int N, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward pass of fa_fwd_varlen (same packed layouts and cu_seqlens table;
+ * dO, dq : bf16 [total, H, d], dk, dv : bf16 [total, Hkv, d], lse from
+ * fa_fwd_varlen).  Each sequence's gradients are those of its own
+ * single-sequence problem.  The workspace is fa_bwd_workspace_bytes(B, H, Hkv,
+ * max_seqlen, d) bytes, as for a batch of B sequences of max_seqlen rows.
+ * Deterministic like fa_bwd.  total = 0 launches nothing. */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dO, void *dq, void *dk, void *dv, const int *cu_seqlens,
+                  int B, int max_seqlen, int total, int H, int Hkv, int d, float scale, int causal,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* The three launches fa_bwd makes, for callers that schedule them separately
  * (same arguments and rules as fa_bwd; run fa_bwd_prepare first, then the
  * other two in either order, on one stream or ordered streams, with the same

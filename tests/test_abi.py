@@ -137,3 +137,18 @@ def test_fwd_varlen_rejects_bad_arguments(lib):
     assert call(H=3) == fa.FA_ERR_INVALID_ARG
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
     assert call(q=A + 8) == fa.FA_ERR_ALIGNMENT
+
+
+def test_bwd_varlen_rejects_bad_arguments(lib):
+    nb = fa.fa_bwd_workspace_bytes(2, 4, 2, 300, 128)
+
+    def call(cu=A, total=400, ws=A, wsb=nb, dq=A, L=300):
+        return fa.fa_bwd_varlen(A, A, A, A, A, A, dq, A, A, cu, 2, L, total, 4, 2, 128, 0.1, 0, ws, wsb, 0)
+
+    assert call(cu=None) == fa.FA_ERR_INVALID_ARG
+    assert call(cu=A + 2) == fa.FA_ERR_INVALID_ARG
+    assert call(total=-3) == fa.FA_ERR_INVALID_ARG
+    assert call(dq=None) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=None) == fa.FA_ERR_WORKSPACE
+    assert call(wsb=nb - 4) == fa.FA_ERR_WORKSPACE
+    assert call(L=0) == fa.FA_ERR_INVALID_ARG

@@ -83,3 +83,56 @@ def test_empty_batch_launches_nothing():
     assert fa.fa_fwd_varlen(A, A, A, A, None, cu, 2, 128, 0, 2, 2, 128, 0.1, 0) == fa.FA_OK
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
+
+
+BWD_CASES = [
+    # lengths, H, Hkv, d, causal
+    ([1, 127, 128, 129, 300, 0, 513], 4, 2, 128, False),
+    ([1, 127, 128, 129, 300, 0, 513], 4, 2, 128, True),
+    ([5, 200, 64, 385], 2, 2, 64, True),
+    ([333, 17, 256], 2, 1, 256, True),
+    ([333, 17, 256], 2, 2, 256, False),
+]
+
+
+@pytest.mark.parametrize("lens,H,Hkv,d,causal", BWD_CASES)
+def test_bwd_matches_oracle(oracle_mod, lens, H, Hkv, d, causal):
+    q, k, v, dO, cu, total = pack(lens, H, Hkv, d, 9500 + sum(lens) + d + causal, with_dO=True)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_fwd_varlen(q, k, v, cu, max(lens), scale=scale, causal=causal)
+    # sentinel rows after `total` in every gradient: nothing may be written there
+    bufs = [with_sentinel(total, q.shape[1], d), with_sentinel(total, k.shape[1], d), with_sentinel(total, k.shape[1], d)]
+    nbytes = fa.fa_bwd_workspace_bytes(len(lens), H, Hkv, max(lens), d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = (b[1] for b in bufs)
+    st = fa.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu, len(lens), max(lens), total, H, Hkv, d, scale, causal,
+                          ws, nbytes)
+    assert st == fa.FA_OK, fa.status_string(st)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for name, (buf, _) in zip(("dQ", "dK", "dV"), bufs):
+        assert (buf[total:] == 7.0).all(), f"{name}: rows past the packed batch were written"
+    ref = oracle_mod.attention_bwd_varlen(q, k, v, dO, cu, scale, causal)
+    bounds = np.concatenate([[0], np.cumsum(lens)])
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        for s_, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+            if b > a:  # per sequence, so one sequence cannot hide in the others' norm
+                check_grad(g[a:b], r[a:b], f"lens {lens} d{d} causal={causal} seq {s_} ({b - a} rows) {name}")
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False), (256, True)])
+def test_bwd_equal_lengths_match_the_fixed_length_path_bitwise(d, causal):
+    B, N, H, Hkv = 2, 300, 4, 2
+    q = inputs.random_bf16((B, N, H, d), 9600 + d, "cuda")
+    k = inputs.random_bf16((B, N, Hkv, d), 9601 + d, "cuda")
+    v = inputs.random_bf16((B, N, Hkv, d), 9602 + d, "cuda")
+    dO = inputs.random_bf16((B, N, H, d), 9603 + d, "cuda")
+    o, lse = fa.attention_fwd(q, k, v, causal=causal)
+    ref = fa.attention_bwd(q, k, v, o, lse, dO, causal=causal)
+    cu = torch.arange(B + 1, dtype=torch.int32, device="cuda") * N
+    flat = lambda x: x.reshape(B * N, x.shape[2], d)
+    lse_v = lse.permute(1, 0, 2).reshape(H, B * N).contiguous()
+    got = fa.attention_bwd_varlen(flat(q), flat(k), flat(v), flat(o), lse_v, flat(dO), cu, N, causal=causal)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
+        assert torch.equal(a.view(torch.int16), flat(b).view(torch.int16)), name
