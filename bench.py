@@ -40,7 +40,8 @@ NOMINAL_BF16_TFLOPS = 2250.0
 def workload(name: str):
     from exact_attention_blackwell_gb300 import inputs
 
-    return {"headline": inputs.headline, "causal": inputs.causal_outliers, "gqa": inputs.long_gqa}[name]()
+    return {"headline": inputs.headline, "causal": inputs.causal_outliers, "gqa": inputs.long_gqa,
+            "varlen": inputs.packed_causal}[name]()
 
 
 def env_int(k, default):
@@ -189,6 +190,8 @@ def run_reference(args):
         return 0
     oracle.build()
     w = workload(args.workload)
+    if args.workload == "varlen":
+        return run_reference_varlen(args, w)
     x = inputs.make_inputs(w, with_dO=w.backward)
     for s in range(args.warmup):
         cpu_oracle_step(x, w, s)
@@ -207,6 +210,36 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_varlen(args, w):
+    """Oracle arm of the packed workload: each step is the shortest sequence's fwd+bwd (all heads)."""
+    import oracle
+    from exact_attention_blackwell_gb300 import inputs
+
+    x = inputs.make_packed_inputs(w)
+    n = min(w.lens)
+    a = w.cu_seqlens()[list(w.lens).index(n)]
+    sl = lambda t: t[None, a:a + n]
+    t = 0.0
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.attention_fwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), w.sm_scale, w.causal)
+        oracle.attention_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["dO"]), w.sm_scale, w.causal)
+        if s >= args.warmup:
+            t += time.perf_counter() - t0
+    f = 3.5 * 4.0 * w.H * n * n * w.d / 2
+    value = f * args.steps / t / 1e12
+    sample = f"the shortest sequence ({n} rows, all {w.H} heads) per step, fwd+bwd, fp64"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + " fwd+bwd", "B": w.B, "total": w.total, "max_seqlen": w.max_seqlen},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
     return 0
 
 
@@ -410,6 +443,135 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ packed variable-length batch
+def run_varlen(args):
+    """One step = fa_fwd_varlen + fa_bwd_varlen on a packed causal batch (single GPU)."""
+    import torch
+
+    import exact_attention_blackwell_gb300 as fa
+    from exact_attention_blackwell_gb300 import inputs
+
+    if env_int("WORLD_SIZE", 1) > 1:
+        raise SystemExit("--workload varlen runs on one GPU")
+    torch.cuda.set_device(0)
+    fa.lib()
+    w = inputs.packed_causal()
+    x_cpu = inputs.make_packed_inputs(w)
+    dev = torch.device("cuda", 0)
+    q, k, v, dO = (x_cpu[n].to(dev) for n in ("q", "k", "v", "dO"))
+    cu = x_cpu["cu_seqlens"].to(dev)
+    B, T, L, H, Hkv, d = w.B, w.total, w.max_seqlen, w.H, w.Hkv, w.d
+    o, lse = torch.empty_like(q), torch.empty((H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nb = fa.fa_bwd_workspace_bytes(B, H, Hkv, L, d)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    fwd_ev, bwd_ev = [], []
+
+    def step(record=False):
+        e = [ev() for _ in range(3)] if record else None
+        if record:
+            e[0].record(stream)
+        st = fa.fa_fwd_varlen(q, k, v, o, lse, cu, B, L, T, H, Hkv, d, w.sm_scale, w.causal, sptr)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_varlen")
+        if record:
+            e[1].record(stream)
+        st = fa.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu, B, L, T, H, Hkv, d, w.sm_scale, w.causal, ws, nb,
+                              sptr)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd_varlen")
+        if record:
+            e[2].record(stream)
+            fwd_ev.append((e[0], e[1]))
+            bwd_ev.append((e[1], e[2]))
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    wall0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
+    clocks = sampler.stop()
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    total_ms = t0.elapsed_time(t1)
+    fwd_f, bwd_f = w.fwd_flops(), w.bwd_flops()
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in bwd_ev)
+    value = (fwd_f + bwd_f) * args.steps / (total_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    # the backward's three launches execute 7 GEMMs of the forward's 2 (S and dP recomputed)
+    achieved = 3.5 * fwd_f / (bwd_ms * 1e-3) / 1e12
+    out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
+           "config": {"workload": w.name + " fwd+bwd", "B": B, "total": T, "max_seqlen": L, "H": H, "Hkv": Hkv,
+                      "d": d, "causal": w.causal, "lens": list(w.lens),
+                      "l2": "inputs larger than L2 (no flush between steps)", "parallelism": "one GPU"},
+           "frac_of_2250_tflops": value / NOMINAL_BF16_TFLOPS,
+           "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
+           "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12, "bwd_ms": bwd_ms,
+           "roofline": {"bound": "tensor", "kernel": "backward (pre + dK/dV + dQ launches)", "achieved": achieved,
+                        "peak": peaks["sustained"], "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
+                        "peak_source": peaks["source"] + ", cuBLAS bf16 sustained",
+                        "flops_per_launch": 3.5 * fwd_f, "launch_ms": bwd_ms, "traffic": None},
+           "gpu_launches": 4 * args.steps, "clocks": clocks}
+    if not args.no_e2e:
+        pin = {n: x_cpu[n].pin_memory() for n in ("q", "k", "v", "dO")}
+        dsts = {"q": q, "k": k, "v": v, "dO": dO}
+        outs = [o, lse, dq, dk, dv]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+
+        def e2e_step():
+            for n, h in pin.items():
+                dsts[n].copy_(h, non_blocking=True)
+            step()
+            for hd, dd in zip(outs_h, outs):
+                hd.copy_(dd, non_blocking=True)
+
+        n_e2e = max(3, args.steps // 2)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        out["e2e"] = {"value": (fwd_f + bwd_f) * n_e2e / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                      "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h), "ms_per_step": ms / n_e2e}
+    if not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        n = min(w.lens)
+        a = w.cu_seqlens()[list(w.lens).index(n)]
+        sl = lambda t: t[None, a:a + n]
+        t_start = time.perf_counter()
+        oracle.attention_fwd(sl(x_cpu["q"]), sl(x_cpu["k"]), sl(x_cpu["v"]), w.sm_scale, w.causal)
+        oracle.attention_bwd(sl(x_cpu["q"]), sl(x_cpu["k"]), sl(x_cpu["v"]), sl(x_cpu["dO"]), w.sm_scale, w.causal)
+        t = time.perf_counter() - t_start
+        f = 3.5 * 4.0 * H * n * n * d / 2
+        out["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                               "kind": "oracle", "seconds": t,
+                               "sample": f"the shortest sequence ({n} rows, all {H} heads), fwd+bwd, fp64"}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,13 +579,17 @@ def main():
                     help="timed steps (default: 100 for our arm, 20 for the CPU oracle arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["headline", "causal", "gqa"], default="headline")
+    ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen"], default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases of the same kernels, e.g. for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, whatever is asked
+    if args.workload == "varlen" and args.impl == "ours":
+        if args.steps is None:
+            args.steps = 100
+        return run_varlen(args)
     if args.steps is None:
         # our arm: about 0.6 s of timed work on the headline workload, long enough for the
         # clock record; the oracle arm: one (batch, head) slice per step, a few seconds each

@@ -12,12 +12,18 @@ Recipe (the pages print no dataset; every workload is synthetic):
     draw per Q element then per K element; an element whose draw is < 0.01 is
     multiplied by 20.
   * Everything is then rounded to bf16 (round-to-nearest-even, torch default).
+  * Packed variable-length batches (``PackedWorkload``): sequence lengths from
+    ``numpy.random.default_rng(seed)``, log-uniform between ``lo`` and ``hi``
+    rows, drawn until ``total`` rows are covered (the last one cut to fit);
+    then Q, K, V, dO as above with shapes [total, H, d] / [total, Hkv, d] from
+    ``torch.Generator().manual_seed(seed)``.
 """
 from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 
@@ -97,3 +103,73 @@ def random_bf16(shape, seed: int, device="cpu"):
     """iid N(0,1) rounded to bf16, for ad-hoc shapes (edge-case tests)."""
     g = torch.Generator().manual_seed(seed)
     return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(device)
+
+
+@dataclass(frozen=True)
+class PackedWorkload:
+    """Sequences of different lengths packed back to back (cu_seqlens layout)."""
+    name: str
+    lens: tuple
+    H: int
+    Hkv: int
+    d: int
+    causal: bool
+    seed: int
+    backward: bool = True
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def total(self) -> int:
+        return int(sum(self.lens))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.lens))
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def cu_seqlens(self) -> list:
+        return [0] + [int(x) for x in np.cumsum(self.lens)]
+
+    def fwd_flops(self) -> float:
+        """Sum over sequences of the single-sequence convention."""
+        f = sum(4.0 * self.H * n * n * self.d for n in self.lens)
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops()
+
+
+def packed_lengths(total: int, lo: int, hi: int, seed: int) -> tuple:
+    rng = np.random.default_rng(seed)
+    lens, left = [], total
+    while left > 0:
+        n = int(round(math.exp(rng.uniform(math.log(lo), math.log(hi)))))
+        n = min(max(n, 1), left)
+        lens.append(n)
+        left -= n
+    return tuple(lens)
+
+
+def packed_causal() -> PackedWorkload:
+    lens = packed_lengths(65536, 128, 16384, 4)
+    return PackedWorkload(f"packed {len(lens)} seqs (128..16384 rows, 65536 total) H16 d128 causal", lens, 16, 16,
+                          128, True, 4)
+
+
+def make_packed_inputs(w: PackedWorkload, device="cpu", with_dO: bool = True):
+    """Returns dict(q, k, v, dO, cu_seqlens) for a packed workload (drawn on the CPU)."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.total, w.H, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.total, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.total, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    dO = torch.randn((w.total, w.H, w.d), generator=g, dtype=torch.float32) if with_dO else None
+    out = {n: (t.to(torch.bfloat16).to(device) if t is not None else None)
+           for n, t in {"q": q, "k": k, "v": v, "dO": dO}.items()}
+    out["cu_seqlens"] = torch.tensor(w.cu_seqlens(), dtype=torch.int32, device=device)
+    return out
