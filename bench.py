@@ -443,6 +443,70 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ FP8 forward
+def run_fp8(args):
+    """One step = fa_fwd_fp8 (rotation + e4m3 quantization launches + the FP8 forward) on the headline shape."""
+    import torch
+
+    import exact_attention_blackwell_gb300 as fa
+    from exact_attention_blackwell_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    fa.lib()
+    w = inputs.headline()
+    x = inputs.make_inputs(w, with_dO=False)
+    dev = torch.device("cuda", 0)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    g = torch.Generator().manual_seed(w.seed)
+    signs = torch.where(torch.rand(d, generator=g) < 0.5, -1.0, 1.0).to(torch.float32).to(dev)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    nb = fa.fa_fwd_fp8_workspace_bytes(B, H, Hkv, N, d)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def step():
+        st = fa.fa_fwd_fp8(q, k, v, signs, o, lse, B, H, Hkv, N, d, w.sm_scale, w.causal, ws, nb, sptr)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_fp8")
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
+    clocks = sampler.stop()
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    ms = t0.elapsed_time(t1) / args.steps
+    f = w.fwd_flops()
+    value = f / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * peaks["sustained"]  # the nominal fp8 : bf16 dense ratio of the part is 2
+    print(json.dumps({
+        "metric": "attention forward TFLOPs/s, FP8 (e4m3) with incoherent processing, d=128, 1 GB300",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": w.name + " fwd, fp8 (rotation and quantization launches included)", "B": B, "H": H,
+                   "Hkv": Hkv, "N": N, "d": d, "causal": w.causal,
+                   "l2": "inputs larger than L2 (no flush between steps)"},
+        "roofline": {"bound": "tensor", "kernel": "fa_fwd_fp8 (3 launches)", "achieved": value, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": value / fp8_peak,
+                     "peak_source": peaks["source"] + ", cuBLAS bf16 sustained x 2 (nominal fp8 / bf16 ratio)",
+                     "traffic": None},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ packed variable-length batch
 def run_varlen(args):
     """One step = fa_fwd_varlen + fa_bwd_varlen on a packed causal batch (single GPU)."""
@@ -579,17 +643,20 @@ def main():
                     help="timed steps (default: 100 for our arm, 20 for the CPU oracle arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen"], default="headline")
+    ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen", "fp8"], default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases of the same kernels, e.g. for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, whatever is asked
-    if args.workload == "varlen" and args.impl == "ours":
+    if args.workload in ("varlen", "fp8") and args.impl == "ours":
         if args.steps is None:
             args.steps = 100
-        return run_varlen(args)
+        return run_varlen(args) if args.workload == "varlen" else run_fp8(args)
+    if args.workload == "fp8":
+        print(json.dumps({"impl": "reference", "unavailable": "the fp8 line has no oracle arm; use the headline workload"}))
+        return 0
     if args.steps is None:
         # our arm: about 0.6 s of timed work on the headline workload, long enough for the
         # clock record; the oracle arm: one (batch, head) slice per step, a few seconds each

@@ -28,6 +28,8 @@ FA_ERR_TIMEOUT = -6
 _P, _I, _F, _LL, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_fp8_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -91,6 +93,16 @@ def status_string(status: int) -> str:
 def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, stream=None) -> int:
     return lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, float(scale),
                         int(bool(causal)), _stream(stream))
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, Hkv, N, d) -> int:
+    return int(lib().fa_fwd_fp8_workspace_bytes(B, H, Hkv, N, d))
+
+
+def fa_fwd_fp8(q, k, v, rot_signs, o, lse, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes,
+               stream=None) -> int:
+    return lib().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(rot_signs), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                            float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale, causal, stream=None) -> int:
@@ -170,6 +182,24 @@ def attention_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
     return o, lse
+
+
+def attention_fwd_fp8(q, k, v, rot_signs=None, scale=None, causal=False, workspace=None, stream=None):
+    """FP8 forward (d = 128): q [B,N,H,128], k/v [B,N,Hkv,128] bf16, rot_signs a float32 CUDA tensor of
+    +-1 [128] or None -> (o bf16, lse fp32 [B,H,N], workspace holding the e4m3 tensors and scales)."""
+    import torch
+
+    B, N, H, Hkv, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = fa_fwd_fp8_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = fa_fwd_fp8(q, k, v, rot_signs, o, lse, B, H, Hkv, N, d, scale, causal, workspace, workspace.numel(), stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
+    return o, lse, workspace
 
 
 def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, out=None, lse=None,

@@ -107,6 +107,38 @@ int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int H
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+int encode_u8_tile_map(CUtensorMap *map, const void *base, const uint64_t dims[4], const uint64_t strides[3],
+                       const uint32_t box_dims[4]) {
+  if (get_encoder() != FA_OK) return FA_ERR_CUDA;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t box[4] = {box_dims[0], box_dims[1], box_dims[2], box_dims[3]};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), d, st, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Workspace of the FP8 forward: the arrays of Fp8PrepParams, each on a 256-byte boundary.
+struct Fp8Layout {
+  size_t q8, k8, vt8, sq, sk, vblk, sv, total;
+};
+Fp8Layout fp8_layout(int B, int H, int Hkv, int N) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t nt = ((size_t)N + 127) / 128, Npad = nt * 128;
+  Fp8Layout l;
+  l.q8 = 0;
+  l.k8 = l.q8 + up((size_t)B * N * H * 128);
+  l.vt8 = l.k8 + up((size_t)B * N * Hkv * 128);
+  l.sq = l.vt8 + up((size_t)B * Hkv * 128 * Npad);
+  l.sk = l.sq + up((size_t)B * H * nt * 4);
+  l.vblk = l.sk + up((size_t)B * Hkv * nt * 4);
+  l.sv = l.vblk + up((size_t)B * Hkv * nt * 4);
+  l.total = l.sv + up((size_t)B * Hkv * 4);
+  return l;
+}
+
 namespace {
 
 __global__ void exp2_poly_kernel(const float *__restrict__ x, float *__restrict__ y, long long n) {
@@ -176,6 +208,77 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
   p.N = max_seqlen;
   p.scale_log2 = scale * 1.4426950408889634f;
   return launch_fwd(p, d, causal != 0, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Hkv, int N, int d) {
+  if (check_common(B, H, Hkv, N, d, 1.0f) != FA_OK || d != 128) return 0;
+  return fp8_layout(B, H, Hkv, N).total;
+}
+
+int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *rot_signs, void *o, float *lse, int B,
+               int H, int Hkv, int N, int d, float scale, int causal, void *workspace, size_t workspace_bytes,
+               void *stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (rot_signs && (reinterpret_cast<uintptr_t>(rot_signs) & 3u)))
+    return FA_ERR_ALIGNMENT;
+  const Fp8Layout l = fp8_layout(B, H, Hkv, N);
+  if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_WORKSPACE;
+  if ((rc = check_device()) != FA_OK) return rc;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const int nt = (N + 127) / 128, Npad = nt * 128;
+  Fp8PrepParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.q = static_cast<const __nv_bfloat16 *>(q);
+  pp.k = static_cast<const __nv_bfloat16 *>(k);
+  pp.v = static_cast<const __nv_bfloat16 *>(v);
+  pp.signs = rot_signs;
+  pp.q8 = ws + l.q8;
+  pp.k8 = ws + l.k8;
+  pp.vt8 = ws + l.vt8;
+  pp.sq = reinterpret_cast<float *>(ws + l.sq);
+  pp.sk = reinterpret_cast<float *>(ws + l.sk);
+  pp.vblk = reinterpret_cast<float *>(ws + l.vblk);
+  pp.sv = reinterpret_cast<float *>(ws + l.sv);
+  pp.B = B;
+  pp.H = H;
+  pp.Hkv = Hkv;
+  pp.N = N;
+  pp.nt = nt;
+  pp.Npad = Npad;
+  Fp8Params p;
+  std::memset(&p, 0, sizeof(p));
+  const uint64_t dq[4] = {128, (uint64_t)H, (uint64_t)N, (uint64_t)B};
+  const uint64_t sq_[3] = {128, (uint64_t)H * 128, (uint64_t)N * H * 128};
+  const uint64_t dk[4] = {128, (uint64_t)Hkv, (uint64_t)N, (uint64_t)B};
+  const uint64_t sk_[3] = {128, (uint64_t)Hkv * 128, (uint64_t)N * Hkv * 128};
+  const uint64_t dv[4] = {(uint64_t)Npad, 128, (uint64_t)Hkv, (uint64_t)B};
+  const uint64_t sv_[3] = {(uint64_t)Npad, (uint64_t)Npad * 128, (uint64_t)Npad * 128 * Hkv};
+  // boxes: 128 rows of one head (128 bytes each) for q8 / k8; 128 head-dim rows x 128 keys for vt8
+  const uint32_t box_rows[4] = {128, 1, 128, 1}, box_vt[4] = {128, 128, 1, 1};
+  if (encode_u8_tile_map(&p.tm_q8, pp.q8, dq, sq_, box_rows) || encode_u8_tile_map(&p.tm_k8, pp.k8, dk, sk_, box_rows) ||
+      encode_u8_tile_map(&p.tm_vt8, pp.vt8, dv, sv_, box_vt))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.sq = pp.sq;
+  p.sk = pp.sk;
+  p.sv = pp.sv;
+  p.status = device_status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.nt = nt;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_fp8_prepare(pp, st)) != FA_OK) return rc;
+  return launch_fwd_fp8(p, causal != 0, st);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {

@@ -8,6 +8,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "../../include/fa.h"
 
 namespace fa {
@@ -102,6 +104,38 @@ __device__ __forceinline__ void work_order(int L, int n_tiles, int n_heads, int 
   head = c * chunk + (r - rank * hc);
 }
 #endif
+
+// FP8 forward (head dim 128).  Prepare: Q, K rotated and quantized to e4m3 per
+// 128-row block of one (batch, head); V quantized per (batch, kv head) and
+// stored transposed.  Layouts (bytes / fp32 arrays, all in the caller's workspace):
+//   q8 [B, N, H, 128], k8 [B, N, Hkv, 128], vt8 [B, Hkv, 128, Npad] (keys contiguous, zero past N),
+//   sq [B, H, nt], sk [B, Hkv, nt], vblk [B, Hkv, nt] (V block maxima), sv [B, Hkv];  nt = Npad / 128.
+struct Fp8PrepParams {
+  const __nv_bfloat16 *q, *k, *v;
+  const float *signs;  // [128] of +-1, or nullptr: no rotation
+  uint8_t *q8, *k8, *vt8;
+  float *sq, *sk, *vblk, *sv;
+  int B, H, Hkv, N, nt, Npad;
+};
+
+struct Fp8Params {
+  CUtensorMap tm_q8, tm_k8, tm_vt8;  // e4m3 tiles of 128 x 128 bytes, 128B swizzle
+  void *o;                            // [B, N, H, 128] bf16
+  float *lse;                         // [B, H, N] or nullptr
+  const float *sq, *sk, *sv;
+  unsigned *status;
+  int B, H, Hkv, N, nt;
+  float scale_log2;
+  int sched_chunk;
+};
+
+int launch_fp8_prepare(const Fp8PrepParams &p, cudaStream_t stream);
+int launch_fwd_fp8(const Fp8Params &p, bool causal, cudaStream_t stream);
+
+// Encodes a 4-D tensor map over bytes (e4m3): dims[0] innermost, strides in
+// bytes for dims 1..3, box extents per dim (box[0] <= 128 bytes), 128-byte swizzle.
+int encode_u8_tile_map(CUtensorMap *map, const void *base, const uint64_t dims[4], const uint64_t strides[3],
+                       const uint32_t box[4]);
 
 // Device status word of the current device (a small static device array).
 unsigned *device_status_ptr();

@@ -85,6 +85,32 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   const int *cu_seqlens, int B, int max_seqlen, int total,
                   int H, int Hkv, int d, float scale, int causal, void *stream);
 
+/* FP8 forward with incoherent processing (FlashAttention-3 page, section 3:
+ * multiply the query and key feature vectors by a random orthogonal matrix,
+ * e.g. a Hadamard matrix, so outlier coordinates spread out, then quantize to
+ * FP8; the orthogonal factor cancels in Q K^T).  Same inputs, outputs and rules
+ * as fa_fwd, for d = 128 only (other head dims: FA_ERR_UNSUPPORTED).
+ *   rot_signs : DEVICE fp32 [128] of +1/-1, the rotation M = diag(rot_signs)
+ *               H_128 / sqrt(128) (H_128 the Sylvester Hadamard matrix) applied
+ *               to every row of q and k; NULL means no rotation.
+ *   The arithmetic: q M and k M rounded to e4m3 (round to nearest even,
+ *   saturating at 448) with one fp32 scale per 128-row block of one (batch,
+ *   head) mapping the block's largest magnitude to 448; v rounded to e4m3 with
+ *   one scale per (batch, kv head); S = Q8 K8^T on the tensor core with fp32
+ *   accumulation; P rounded to e4m3 for P V8; the row sum and LSE from the
+ *   unrounded P in fp32; o written in bf16.
+ *   workspace : caller-owned device memory, 256-byte aligned, of at least
+ *     fa_fwd_fp8_workspace_bytes() bytes; it receives, each on a 256-byte
+ *     boundary and in this order, q8 [B,N,H,128] and k8 [B,N,Hkv,128] (e4m3),
+ *     vt8 [B,Hkv,128,Npad] (e4m3, keys contiguous, zero past N), the fp32
+ *     scales sq [B,H,nt], sk [B,Hkv,nt], the V block maxima [B,Hkv,nt] and sv
+ *     [B,Hkv] (Npad = nt * 128, nt = ceil(N / 128)).
+ * Three launches on `stream`. */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Hkv, int N, int d);
+int fa_fwd_fp8(const void *q, const void *k, const void *v, const float *rot_signs, void *o, float *lse,
+               int B, int H, int Hkv, int N, int d, float scale, int causal,
+               void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of device workspace fa_bwd needs for these sizes: two fp32 row-term
  * arrays [B,H,Npad] (D = rowsum(dO * O) and the log2-scaled LSE), Npad = N
  * rounded up to a multiple of 128, each starting on a 256-byte boundary.

@@ -152,3 +152,18 @@ def test_bwd_varlen_rejects_bad_arguments(lib):
     assert call(ws=None) == fa.FA_ERR_WORKSPACE
     assert call(wsb=nb - 4) == fa.FA_ERR_WORKSPACE
     assert call(L=0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fwd_fp8_rejects_bad_arguments(lib):
+    nb = fa.fa_fwd_fp8_workspace_bytes(1, 2, 2, 256, 128)
+    assert nb > 0 and fa.fa_fwd_fp8_workspace_bytes(1, 2, 2, 256, 64) == 0
+
+    def call(d=128, ws=A, wsb=nb, q=A, signs=None):
+        return fa.fa_fwd_fp8(q, A, A, signs, A, None, 1, 2, 2, 256, d, 0.1, 0, ws, wsb, 0)
+
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(q=None) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=None) == fa.FA_ERR_WORKSPACE
+    assert call(wsb=nb - 1) == fa.FA_ERR_WORKSPACE
+    assert call(ws=A + 16) == fa.FA_ERR_WORKSPACE  # 256-byte alignment
+    assert call(signs=A + 2) == fa.FA_ERR_ALIGNMENT
