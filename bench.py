@@ -398,33 +398,76 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return 0
-    pin = {n: x_cpu[n].pin_memory() for n in ("q", "k", "v") + (("dO",) if w.backward else ())}
-    outs_d = [o, lse] + ([dq, dk, dv] if w.backward else [])
-    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_d]
-    dsts = {"q": q, "k": k, "v": v, "dO": dO}
+    # Pipelined over three streams, as a caller feeding a stream of batches would
+    # run it: step i's uploads (stream s_in) overlap step i-1's kernels (s_cmp)
+    # and step i-2's downloads (s_out); two device buffer sets alternate.  Every
+    # step still moves its full inputs host -> device and outputs device -> host.
+    names = ("q", "k", "v") + (("dO",) if w.backward else ())
+    pin = {n: x_cpu[n].pin_memory() for n in names}
+    first_in = {"q": q, "k": k, "v": v, "dO": dO}
+    first_out = [o, lse] + ([dq, dk, dv] if w.backward else [])
+    sets = [({n: first_in[n] for n in names}, first_out),
+            ({n: torch.empty_like(first_in[n]) for n in names}, [torch.empty_like(t) for t in first_out])]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in first_out]
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for n, h in pin.items():
-            dsts[n].copy_(h, non_blocking=True)
-        step()
-        for hd, dd in zip(outs_h, outs_d):
-            hd.copy_(dd, non_blocking=True)
+    def kernels(ins, outs, sp):
+        check(fa.fa_fwd(ins["q"], ins["k"], ins["v"], outs[0], outs[1], B, H, Hkv, N, d, scale, causal, sp), "fa_fwd")
+        if w.backward:
+            check(fa.fa_bwd_prepare(outs[0], outs[1], ins["dO"], B, H, Hkv, N, d, ws, ws_bytes, sp), "fa_bwd_prepare")
+            check(fa.fa_bwd_dkdv(ins["q"], ins["k"], ins["v"], ins["dO"], outs[3], outs[4], B, H, Hkv, N, d, scale,
+                                 causal, ws, ws_bytes, sp), "fa_bwd_dkdv")
+            check(fa.fa_bwd_dq(ins["q"], ins["k"], ins["v"], ins["dO"], outs[2], B, H, Hkv, N, d, scale, causal, ws,
+                               ws_bytes, sp), "fa_bwd_dq")
+
+    def pipeline(n_steps, e_start=None, e_end=None):
+        in_done, cmp_done, out_done = [], [], []
+        if e_start is not None:
+            e_start.record(s_in)
+        for i in range(n_steps):
+            ins, outs = sets[i % 2]
+            if i >= 2:
+                s_in.wait_event(cmp_done[i - 2])  # step i-2 has finished reading this input set
+            with torch.cuda.stream(s_in):
+                for n in names:
+                    ins[n].copy_(pin[n], non_blocking=True)
+            in_done.append(torch.cuda.Event())
+            in_done[-1].record(s_in)
+            s_cmp.wait_event(in_done[i])
+            if i >= 2:
+                s_cmp.wait_event(out_done[i - 2])  # step i-2's outputs in this set are on the host
+            kernels(ins, outs, s_cmp.cuda_stream)
+            cmp_done.append(torch.cuda.Event())
+            cmp_done[-1].record(s_cmp)
+            s_out.wait_event(cmp_done[i])
+            with torch.cuda.stream(s_out):
+                for hd, dd in zip(outs_h, outs):
+                    hd.copy_(dd, non_blocking=True)
+            out_done.append(torch.cuda.Event())
+            out_done[-1].record(s_out)
+        if e_end is not None:
+            for e in out_done + cmp_done:
+                s_out.wait_event(e)
+            e_end.record(s_out)
 
     e2e_steps = max(3, args.steps // 2)
-    for _ in range(2):
-        e2e_step()
+    torch.cuda.synchronize()
+    pipeline(3)
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    pipeline(e2e_steps, e0, e1)
     torch.cuda.synchronize()
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait (end-to-end leg)")
     e2e_ms = sharding.max_over_ranks(e0.elapsed_time(e1), dist, dev)
     out["e2e"] = {"value": sharding.whole_job_tflops(step_f, e2e_steps, e2e_ms, world), "unit": "TFLOP/s",
                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h),
-                  "ms_per_step": e2e_ms / e2e_steps}
+                  "ms_per_step": e2e_ms / e2e_steps,
+                  "schedule": "three streams: uploads of step i, kernels of step i-1, downloads of step i-2 overlap; "
+                              "two device buffer sets"}
+    if not torch.equal(outs_h[0], first_out[0].cpu()) and not torch.equal(outs_h[0], sets[1][1][0].cpu()):
+        raise RuntimeError("end-to-end output differs from the device result")
 
     # ---- CPU oracle on the host cores (rank 0, single GPU only), a bounded sample
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
