@@ -76,55 +76,67 @@ __device__ unsigned long long g_cta[2][65536][3];
 #endif
 
 // ------------------------------------------------------------------ pre
-template <int E> struct BfVec;  // E bf16 values loaded at once
-template <> struct BfVec<2> { using T = uint32_t; };
-template <> struct BfVec<4> { using T = uint2; };
-template <> struct BfVec<8> { using T = uint4; };
+// Rows (b, n, h) of the padded range n < Npad.  A row of D bf16 is read as
+// D / 8 16-byte chunks by D / 8 consecutive lanes, so a warp covers 32 / (D / 8)
+// rows at a time; each warp takes kPreIters such groups and issues all of its
+// loads before it reduces.  With a varlen table (cu != nullptr) the rows of
+// sequence b are packed at its offset and lse is [H, total].
+constexpr int kPreIters = 4;
 
-// One warp per row (b, n, h) of the padded range n < Npad; lane l holds
-// elements [l E, l E + E) of the row.  With a varlen table (cu != nullptr) the
-// rows of sequence b are packed at its offset and lse is [H, total].
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
                                                       float *__restrict__ delta, int B, int H, int N, int Npad,
                                                       const int *__restrict__ cu, int total) {
-  constexpr int E = D / 32;
-  using V = typename BfVec<E>::T;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int L = D / 8;      // lanes per row
+  constexpr int RPW = 32 / L;   // rows per warp per iteration
   const int lane = threadIdx.x & 31;
-  if (row >= (long long)B * Npad * H) return;
-  const int h = (int)(row % H);
-  const long long bn = row / H;
-  const int n = (int)(bn % Npad);
-  const int b = (int)(bn / Npad);
-  const size_t rw = ((size_t)b * H + h) * Npad + n;
-  const SeqSpan sq = seq_span(cu, b, N, total);
-  if (n >= sq.len) {
-    if (lane == 0) {
-      lse2[rw] = INFINITY;  // padded query rows: P = 2^(s - inf) = 0
-      delta[rw] = 0.f;
+  const int sub = lane / L, part = lane % L;
+  const long long rows = (long long)B * Npad * H;
+  const long long base = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPW * kPreIters);
+  uint4 va[kPreIters], vg[kPreIters];
+  long long rw_[kPreIters];
+  bool live[kPreIters];
+  size_t lse_i[kPreIters];
+#pragma unroll
+  for (int it = 0; it < kPreIters; ++it) {
+    const long long row = base + it * RPW + sub;
+    live[it] = false;
+    rw_[it] = -1;
+    va[it] = vg[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (row >= rows) continue;
+    const int h = (int)(row % H);
+    const long long bn = row / H;
+    const int n = (int)(bn % Npad);
+    const int b = (int)(bn / Npad);
+    rw_[it] = ((long long)b * H + h) * Npad + n;
+    const SeqSpan sq = seq_span(cu, b, N, total);
+    if (n >= sq.len) continue;  // padded query row
+    live[it] = true;
+    const size_t grow = cu ? (size_t)sq.start + n : (size_t)b * N + n;  // row in the [rows, H, D] tensors
+    lse_i[it] = cu ? (size_t)h * total + sq.start + n : ((size_t)b * H + h) * N + n;
+    const size_t off = (grow * H + h) * D + part * 8;
+    va[it] = *reinterpret_cast<const uint4 *>(o + off);
+    vg[it] = *reinterpret_cast<const uint4 *>(dO + off);
+  }
+#pragma unroll
+  for (int it = 0; it < kPreIters; ++it) {
+    const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&va[it]);
+    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&vg[it]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      acc = fmaf(__low2float(a2[w]), __low2float(g2[w]), acc);
+      acc = fmaf(__high2float(a2[w]), __high2float(g2[w]), acc);
     }
-    return;
-  }
-  const size_t grow = cu ? (size_t)sq.start + n : (size_t)b * N + n;  // row in the [rows, H, D] tensors
-  const size_t off = (grow * H + h) * D + lane * E;
-  const V va = *reinterpret_cast<const V *>(o + off);
-  const V vg = *reinterpret_cast<const V *>(dO + off);
-  const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
-  const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&vg);
-  float acc = 0.f;
 #pragma unroll
-  for (int w = 0; w < E / 2; ++w) {
-    acc = fmaf(__low2float(a2[w]), __low2float(g2[w]), acc);
-    acc = fmaf(__high2float(a2[w]), __high2float(g2[w]), acc);
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    lse2[rw] = lse[cu ? (size_t)h * total + sq.start + n : ((size_t)b * H + h) * N + n] * kLog2e;
-    delta[rw] = acc;
+    for (int s = L / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (part == 0 && rw_[it] >= 0) {
+      // padded query rows: LSE2 = +inf gives P = 2^(s - inf) = 0, and D = 0
+      lse2[rw_[it]] = live[it] ? lse[lse_i[it]] * kLog2e : INFINITY;
+      delta[rw_[it]] = live[it] ? acc : 0.f;
+    }
   }
 }
 
@@ -1393,7 +1405,8 @@ template <int D>
 int launch_pre_t(const BwdParams &p, const void *o, const void *dO, const float *lse, cudaStream_t stream) {
   const int Npad = (p.N + 127) / 128 * 128;
   const long long rows = (long long)p.B * Npad * p.H;
-  bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+  const long long rows_per_block = 8LL * (32 / (D / 8)) * kPreIters;  // 8 warps
+  bwd_pre_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, p.lse2,
       const_cast<float *>(p.delta), p.B, p.H, p.N, Npad, p.cu_seqlens, p.total);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
