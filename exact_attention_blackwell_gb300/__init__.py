@@ -40,6 +40,7 @@ SIGNATURES = {
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_exp2_poly": (_I, [_P, _P, _LL, _P]),
     "fa_last_device_status": (_I, [_P]),
+    "fa_rescale_count": (_I, [_P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -157,6 +158,15 @@ FA_BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 def fa_exp2_poly(x, y, n, stream=None) -> int:
     return lib().fa_exp2_poly(_ptr(x), _ptr(y), int(n), _stream(stream))
+
+
+def fa_rescale_count(stream=None) -> int:
+    """Rescales applied by the forward kernels since the last call (then reset)."""
+    c = ctypes.c_uint(0)
+    st = lib().fa_rescale_count(_stream(stream), ctypes.addressof(c))
+    if st != FA_OK:
+        raise FaError(st, "fa_rescale_count")
+    return int(c.value)
 
 
 def fa_last_device_status(stream=None) -> int:

@@ -502,6 +502,19 @@ int fa_last_device_status(void *stream) {
   return FA_OK;
 }
 
+int fa_rescale_count(void *stream, unsigned *count) {
+  if (!count) return FA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned *st = device_status_ptr();
+  if (!st) return FA_ERR_CUDA;
+  unsigned h = 0;
+  if (cudaMemcpy(&h, st + 2, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(st + 2, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  *count = h;
+  return FA_OK;
+}
+
 const char *fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";

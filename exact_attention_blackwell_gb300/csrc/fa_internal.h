@@ -22,8 +22,13 @@ namespace fa {
 
 // Conditional-rescale threshold tau, log2 units (FlashAttention-4 paper
 // summary, section 2.B: rescale only when the running maximum moves by more
-// than a threshold; the pages give no value).
-constexpr float kRescaleTau = 8.0f;
+// than a threshold; the pages give no value).  A build-time define so that a
+// tau = 0 build (rescale whenever the maximum moves) can be checked against the
+// default; the result is the same up to rounding for every tau.
+#ifndef FA_RESCALE_TAU
+#define FA_RESCALE_TAU 8.0f
+#endif
+constexpr float kRescaleTau = FA_RESCALE_TAU;
 
 struct FwdParams {
   CUtensorMap tm_q;  // [B, N, H, d] bf16, box 128 rows x 64 cols, 128B swizzle

@@ -196,6 +196,14 @@ int fa_exp2_poly(const float *x, float *y, long long n, void *stream);
  * call (and clears the flag).  Returns FA_ERR_CUDA if synchronisation fails. */
 int fa_last_device_status(void *stream);
 
+/* Debugging aid: how many times a warp of the forward kernels applied the
+ * conditional O rescale (FlashAttention-4 paper summary, section 2.B: rescale
+ * only when the running maximum moves past a threshold) since the last call on
+ * this device; the counter is then reset.  Synchronizes `stream` first.
+ * count: host pointer, written on FA_OK.  Returns FA_ERR_INVALID_ARG for a
+ * NULL count and FA_ERR_CUDA if synchronisation or the copy fails. */
+int fa_rescale_count(void *stream, unsigned *count);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *fa_status_string(int status);
 

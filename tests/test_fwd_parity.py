@@ -62,10 +62,13 @@ def test_small_shapes_full(oracle_mod, B, N, H, Hkv, d, causal):
 
 
 def test_outliers_force_rescale(oracle_mod):
-    """x20 outliers in Q and K move row maxima by far more than the rescale threshold."""
+    """x20 outliers in Q and K move row maxima by far more than the rescale threshold:
+    the conditional rescale must fire (counter > 0) and the result stay exact."""
     w = inputs.Workload("outliers", 1, 2, 2, 1024, 128, True, 7, outliers=True)
     x = inputs.make_inputs(w)
+    fa.fa_rescale_count()  # reset
     o, lse = run_fwd(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
+    assert fa.fa_rescale_count() > 0
     o_ref, lse_ref = oracle_mod.attention_fwd(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
     check_o(o, o_ref, w.name)
     check_lse(lse, lse_ref, w.name)
