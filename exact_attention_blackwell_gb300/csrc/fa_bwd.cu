@@ -205,6 +205,41 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
   return false;
 }
 
+// P^T = 2^(S^T c - LSE2) for one key row and 64 query columns, kept in pe
+// (fp32) and stored to TMEM as bf16 for the dV MMA.  MASK is a template
+// argument so that unmasked tiles run a branch-free body; the caller picks it
+// uniformly per warp (tcgen05.st is warp-collective), and the masked body zeroes
+// key rows past the sequence and, on the causal diagonal tile (diag), keys after
+// the query.
+template <bool MASK>
+__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[64], const float *lse2_s,
+                                       float scale_log2, int wg, int r, bool row_valid, bool diag, uint32_t p_tm) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
+      float x[4];
+      ffma2(x[0], x[1], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]), scale_log2, scale_log2, -l4.x,
+            -l4.y);
+      ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), scale_log2, scale_log2, -l4.z,
+            -l4.w);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
+      if (MASK) {
+        const int qc = 64 * wg + 32 * c + k;  // query column within tile i
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (!row_valid || (diag && qc + u < r)) pe[32 * c + k + u] = 0.f;
+      }
+      w[k >> 1] = pack_bf16x2(pe[32 * c + k], pe[32 * c + k + 1]);
+      w[(k >> 1) + 1] = pack_bf16x2(pe[32 * c + k + 2], pe[32 * c + k + 3]);
+    }
+    tmem_st_32x32b_x16(p_tm + 16 * c, w);
+  }
+}
+
 // Key-row elementwise work of the dK/dV kernels over all iterations: one thread
 // per key row (TMEM lane), warpgroup wg owns query columns [64 wg, 64 wg + 64).
 //   P^T  = 2^(S^T c - LSE2), masked -> registers (fp32) and TMEM over S^T (bf16, dV's A operand)
@@ -223,6 +258,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
   const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
   const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
   const bool row_valid = kv0 + r < L;  // key rows past the sequence: P = 0
+  const bool warp_has_invalid = __any_sync(0xffffffffu, !row_valid);
   bool ok = true;
   for (int it = 0; it < n_iter && ok; ++it) {
     const int rs = it % C::kRowStages;
@@ -235,37 +271,18 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
     tc_fence_after();
-    const bool need_mask = !row_valid || (CAUSAL && i == jt);  // key rows past N, or the diagonal tile
+    const bool diag = CAUSAL && i == jt;
+    const bool need_mask = warp_has_invalid || diag;  // uniform across the warp
     uint32_t sv[2][32];
     tmem_ld_32x32b_x32(s_tm, sv[0]);
     tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
     tmem_wait_ld(sv[0]);
     reg_tie(sv[1]);
     float pe[64];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint32_t w[16];
-#pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + 32 * c + k);
-        float x[4];
-        ffma2(x[0], x[1], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]), p.scale_log2, p.scale_log2,
-              -l4.x, -l4.y);
-        ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), p.scale_log2,
-              p.scale_log2, -l4.z, -l4.w);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
-        if (need_mask) {
-          const int qc = 64 * wg + 32 * c + k;  // query column within tile i
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (!row_valid || qc + u < r) pe[32 * c + k + u] = 0.f;
-        }
-        w[k >> 1] = pack_bf16x2(pe[32 * c + k], pe[32 * c + k + 1]);
-        w[(k >> 1) + 1] = pack_bf16x2(pe[32 * c + k + 2], pe[32 * c + k + 3]);
-      }
-      tmem_st_32x32b_x16(p_tm + 16 * c, w);
-    }
+    if (need_mask)
+      dkdv_p<true>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, p_tm);
+    else
+      dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, p_tm);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(bar(C::kBarP));
