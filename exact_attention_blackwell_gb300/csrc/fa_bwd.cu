@@ -330,6 +330,21 @@ struct DkdvCfg {
   // dO_i = fill 2i + 1), so loads run more than two iterations ahead; the
   // per-iteration LSE2 / D rows go through their own small ring.
   static constexpr int kSlots = (D == 64) ? 10 : 5;
+  // Q and dO have rings of their own: a Q slot is released when dK_i completes,
+  // a dO slot when dV_i does (earlier), so each load gets more than a load
+  // latency of lead.  (One shared round-robin ring tied every dO load to the dK
+  // of two iterations back and left it short of its latency.)
+  static constexpr int kQSlots = (3 * kSlots + 4) / 5;  // 5 -> 3, 10 -> 6
+  static constexpr int kDoSlots = kSlots - kQSlots;
+  // fill 2 i = Q_i, fill 2 i + 1 = dO_i
+  __device__ static int slot(int fill) {
+    const int i = fill >> 1;
+    return (fill & 1) ? kQSlots + i % kDoSlots : i % kQSlots;
+  }
+  __device__ static uint32_t phase(int fill) {
+    const int i = fill >> 1;
+    return (uint32_t)(((fill & 1) ? i / kDoSlots : i / kQSlots) & 1);
+  }
   static constexpr int kRowStages = 2;  // own full/empty barriers, released after each dS
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8, kLoadWarp = 9;
@@ -456,11 +471,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);        // K-major view
       const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);   // MN-major view
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
-      auto slot_of = [](int fill) { return fill % C::kSlots; };
+      auto slot_of = [](int fill) { return C::slot(fill); };
       auto soff = [&](int fill) { return (uint64_t)((slot_of(fill) * C::kTile) >> 4); };
       auto full_ok = [&](int fill) {
-        return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kSlots) & 1), wctx,
-                              kBSiteFull);
+        return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), C::phase(fill), wctx, kBSiteFull);
       };
       auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it)
         if (elect_one()) {
@@ -565,8 +579,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
         const int hh = kh * g + it / per_head;
         const int i = i_start + it % per_head;
         for (int t = 0; t < 2 && ok; ++t, ++fill) {  // t = 0: Q_it, t = 1: dO_it
-          const int s = fill % C::kSlots;
-          ok = mbar_wait(bar(C::kBarEmpty0 + s), ((fill / C::kSlots) & 1) ^ 1, wctx, kBSiteEmpty);
+          const int s = C::slot(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
           if (!ok) break;
           const uint32_t fb = bar(C::kBarFull0 + s);
           mbar_arrive_expect_tx(fb, C::kTile);
@@ -574,6 +588,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
           for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, sq.start + i * 128, sq.bc,
                              keep);
+          FA_TRACE_EV(0, it, 4 + t);
         }
         if (!ok) break;
         // LSE2 / D rows of iteration it, into row stage it % kRowStages once the
@@ -587,11 +602,17 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
         const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
         bulk_load(rdst, p.lse2 + roff, 512, rb);
         bulk_load(rdst + 512, p.delta + roff, 512, rb);
+        FA_TRACE_EV(0, it, 6);
         ++rows_issued;
       }
       const uint64_t t0 = global_timer_ns();
-      for (int f = max(0, fill - C::kSlots); f < fill; ++f)
-        while (!mbar_test(bar(C::kBarFull0 + f % C::kSlots), (f / C::kSlots) & 1) &&
+      // the last issued fill of each slot: Q_i for the last kQSlots i issued, dO_i for the last kDoSlots
+      const int nq = (fill + 1) / 2, nd = fill / 2;
+      for (int i = max(0, nq - C::kQSlots); i < nq; ++i)
+        while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * i)), C::phase(2 * i)) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+      for (int i = max(0, nd - C::kDoSlots); i < nd; ++i)
+        while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * i + 1)), C::phase(2 * i + 1)) &&
                global_timer_ns() - t0 < kWaitLimitNs) {}
       for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
         while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
