@@ -15,6 +15,7 @@
 #pragma once
 
 #include "exp2_poly_coeffs.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -35,6 +36,25 @@ __device__ __forceinline__ float exp2_poly(float x) {
   const float p = __fmaf_rn(__fmaf_rn(__fmaf_rn(FA_EXP2_C3, f, FA_EXP2_C2), f, FA_EXP2_C1), f, 1.0f);
   const int bits = __float_as_int(p) + (__float_as_int(t) << 23);  // p * 2^(j + 64)
   return mul_rn_noftz(__int_as_float(bits), 0x1p-64f);
+}
+
+// Two values with f32x2 arithmetic: the same operations as exp2_poly, each
+// rounded once (x - j as fma(j, -1, x)), so each result equals exp2_poly of its
+// input bit for bit in half the floating-point instructions.
+__device__ __forceinline__ void exp2_poly2(float x0, float x1, float &y0, float &y1) {
+  constexpr float kShift = 12582912.0f + 64.0f;
+  x0 = fmaxf(x0, -150.0f);
+  x1 = fmaxf(x1, -150.0f);
+  float t0, t1, j0, j1, f0, f1, p0, p1;
+  fadd2(t0, t1, x0, x1, kShift, kShift);
+  fadd2(j0, j1, t0, t1, -kShift, -kShift);
+  ffma2(f0, f1, j0, j1, -1.0f, -1.0f, x0, x1);
+  ffma2(p0, p1, FA_EXP2_C3, FA_EXP2_C3, f0, f1, FA_EXP2_C2, FA_EXP2_C2);
+  ffma2(p0, p1, p0, p1, f0, f1, FA_EXP2_C1, FA_EXP2_C1);
+  ffma2(p0, p1, p0, p1, f0, f1, 1.0f, 1.0f);
+  const int b0 = __float_as_int(p0) + (__float_as_int(t0) << 23);
+  const int b1 = __float_as_int(p1) + (__float_as_int(t1) << 23);
+  fmul2(y0, y1, __int_as_float(b0), __int_as_float(b1), 0x1p-64f, 0x1p-64f);
 }
 
 }  // namespace fa

@@ -25,8 +25,15 @@
 // by columns (64 each), one thread per TMEM lane; warp 8 MMA issue; warp 9 TMA.
 #include <cuda_bf16.h>
 
+#include "exp2_poly.cuh"
 #include "fa_internal.h"
 #include "ptx.cuh"
+
+// Share of the dK/dV kernel's exponentials taken on the FMA pipe (exp2_poly2):
+// columns with (column % 16) < FA_BWD_POLY_PER16; even, 0 = all on MUFU.EX2.
+#ifndef FA_BWD_POLY_PER16
+#define FA_BWD_POLY_PER16 0
+#endif
 
 namespace fa {
 namespace {
@@ -211,7 +218,7 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
 // uniformly per warp (tcgen05.st is warp-collective), and the masked body zeroes
 // key rows past the sequence and, on the causal diagonal tile (diag), keys after
 // the query.
-template <bool MASK>
+template <bool MASK, int POLY16 = FA_BWD_POLY_PER16>
 __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[64], const float *lse2_s,
                                        float scale_log2, int wg, int r, bool row_valid, bool diag, uint32_t p_tm) {
 #pragma unroll
@@ -225,8 +232,16 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[
             -l4.y);
       ffma2(x[2], x[3], __uint_as_float(sv[c][k + 2]), __uint_as_float(sv[c][k + 3]), scale_log2, scale_log2, -l4.z,
             -l4.w);
+      static_assert(POLY16 % 2 == 0, "pairs of columns share one packed evaluation");
 #pragma unroll
-      for (int u = 0; u < 4; ++u) pe[32 * c + k + u] = ex2_mufu(x[u]);
+      for (int u = 0; u < 4; u += 2) {
+        if ((32 * c + k + u) % 16 < POLY16) {
+          exp2_poly2(x[u], x[u + 1], pe[32 * c + k + u], pe[32 * c + k + u + 1]);
+        } else {
+          pe[32 * c + k + u] = ex2_mufu(x[u]);
+          pe[32 * c + k + u + 1] = ex2_mufu(x[u + 1]);
+        }
+      }
       if (MASK) {
         const int qc = 64 * wg + 32 * c + k;  // query column within tile i
 #pragma unroll

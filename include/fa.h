@@ -182,13 +182,16 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    const void *dO, void *dq, void *dk, void *dv,
                    int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
 
-/* The software 2^x the forward kernel evaluates on the FMA pipe (FlashAttention-4
+/* The software 2^x the kernels evaluate on the FMA pipe (FlashAttention-4
  * paper summary, section 2.B: 2^x emulated with FMA instructions, a polynomial
  * of degree 3 to 5 for the fractional part).  Range reduction x = j + f with
  * j = rint(x), |f| <= 1/2; a degree-3 minimax polynomial for 2^f; 2^j inserted
  * into the exponent.  Evaluates y[i] = 2^x[i] for n fp32 values on `stream`
  * (device pointers, 4-byte aligned).  Valid for x <= 63; x below -150 or -inf
- * gives +0.  Exposed so that its accuracy can be checked exhaustively. */
+ * gives +0.  Exposed so that its accuracy can be checked exhaustively.  The
+ * kernels evaluate it either one value at a time (forward) or two at a time in
+ * f32x2 arithmetic (dK/dV); this entry point computes both forms and returns
+ * NaN for an element where they differ in any bit. */
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream);
 
 /* Synchronises `stream`, then returns FA_OK or FA_ERR_TIMEOUT if a bounded wait
