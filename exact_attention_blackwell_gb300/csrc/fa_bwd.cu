@@ -300,7 +300,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
       dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, p_tm);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(bar(C::kBarP));
+    mbar_arrive_warp(bar(C::kBarP));
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
     // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
     ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
@@ -330,8 +330,8 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(bar(C::kBarDS));
-    mbar_arrive(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
+    mbar_arrive_warp(bar(C::kBarDS));
+    mbar_arrive_warp(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
   }
   return ok;
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
       const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
-      mbar_init(bar(i), all ? 256u : 1u);
+      mbar_init(bar(i), all ? 8u : 1u);  // one arrival per elementwise warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -671,7 +671,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
     tmem_wait_ld(sv[0]);
     reg_tie(sv[1]);
     tc_fence_before();
-    mbar_arrive(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
+    mbar_arrive_warp(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
     const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
     const int lim = (CAUSAL ? min(q_row, L - 1) : L - 1) - kvc0;  // last visible column offset
     float pe[64];
@@ -708,7 +708,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
     tmem_st_32x32b_x32(ds_tm, w);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(bar(C::kBarDS));
+    mbar_arrive_warp(bar(C::kBarDS));
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
   }
   return ok;
@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarQdo || i == C::kBarSFree || i == C::kBarDS) ? 256u : 1u);
+      mbar_init(bar(i), (i == C::kBarQdo || i == C::kBarSFree || i == C::kBarDS) ? 8u : 1u);  // per elementwise warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -818,7 +818,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarQdo));
+      mbar_arrive_warp(bar(C::kBarQdo));
       if (threadIdx.x == 0) FA_LIFE(1, 2);
     }
     const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
@@ -1059,7 +1059,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
       const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
-      mbar_init(bar(i), all ? 256u : 1u);
+      mbar_init(bar(i), all ? 8u : 1u);  // one arrival per elementwise warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -1290,7 +1290,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
   auto slot_of = [](int fill) { return fill % C::kSlots; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNumBars; ++i) mbar_init(bar(i), (i == C::kBarSFree || i == C::kBarDS) ? 256u : 1u);
+    for (int i = 0; i < C::kNumBars; ++i)  // per elementwise warp
+      mbar_init(bar(i), (i == C::kBarSFree || i == C::kBarDS) ? 8u : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }

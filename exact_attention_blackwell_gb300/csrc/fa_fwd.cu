@@ -150,11 +150,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   }
 
   if (threadIdx.x == 0) {
-    // p_full[t] collects one arrival per softmax thread; every other barrier one.
+    // p_full[t] collects one arrival per softmax warp; every other barrier one.
     for (int i = 0; i < C::kNumBars; ++i) {
       const uint32_t bar = bar0 + 8u * i;
       const bool is_p = bar >= p_bar(0) && bar < p_bar(0) + 8u * QT;
-      mbar_init(bar, is_p ? 128u : 1u);
+      mbar_init(bar, is_p ? 4u : 1u);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
       l_sum += (l0 + l1) + (l2 + l3);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_bar(t));
+      mbar_arrive_warp(p_bar(t));
       if (r == 0) FA_TRACE_EV(j, 3 + 4 * t);
     }
 

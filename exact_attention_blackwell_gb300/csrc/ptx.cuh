@@ -71,6 +71,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// One arrival per warp: the warp barrier orders every lane's earlier work (TMEM
+// stores fenced with tcgen05.fence::before_thread_sync, shared-memory reads)
+// before lane 0's release-arrive.  Barriers that collect these are initialised
+// with a count of warps, not threads; fewer updates of the barrier word reach
+// the waiting warp sooner.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Every wait in the kernels is bounded.  When a wait runs out, the CTA's abort
 // flag (shared memory) and the library's device status word are set, and the
 // caller unwinds without touching the pipeline again.  Other waits in the same
