@@ -124,6 +124,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ peaks and profiles
+# The roofline's denominator: each timed region lasts well under a second and
+# its SM clock stays near the maximum, the conditions of the burst GEMM figure;
+# the sustained figure (seconds of back-to-back GEMMs at the 1.4 kW cap, SM
+# clock ~1450 MHz) is reported beside it as frac_of_sustained.
+PEAK_NOTE = "cuBLAS bf16 burst (timed region under a second, SM clock near max)"
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -369,12 +376,13 @@ def run_ours(args):
         kern = ("bwd_dkdv_kernel", dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
             ("bwd_dq_kernel", dq_ms, 3 * gemm, "fa_bwd.cu")
         name, kms, kflops, _ = kern
-        src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "fa_internal.h"])
+        src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
         achieved = kflops / (kms * 1e-3) / 1e12
         out["roofline"] = {
             "bound": "tensor", "kernel": name, "achieved": achieved,
-            "peak": peaks["sustained"], "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
-            "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
+            "peak": peaks["burst"], "unit": "TFLOP/s", "frac": achieved / peaks["burst"],
+            "frac_of_sustained": achieved / peaks["sustained"],
+            "peak_source": peaks["source"] + ", " + PEAK_NOTE,
             "flops_per_launch": kflops, "launch_ms": kms,
             "traffic": profiled_traffic(f"{name}_{args.workload}.md", src),
         }
@@ -382,9 +390,9 @@ def run_ours(args):
         src = kernel_source_hash(["fa_fwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
         achieved = fwd_f / (fwd_ms * 1e-3) / 1e12
         out["roofline"] = {
-            "bound": "tensor", "kernel": "fa_fwd_kernel", "achieved": achieved, "peak": peaks["sustained"],
-            "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
-            "peak_source": peaks["source"] + ", cuBLAS bf16 sustained (kernel timed inside a long step)",
+            "bound": "tensor", "kernel": "fa_fwd_kernel", "achieved": achieved, "peak": peaks["burst"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["burst"], "frac_of_sustained": achieved / peaks["sustained"],
+            "peak_source": peaks["source"] + ", " + PEAK_NOTE,
             "flops_per_launch": fwd_f, "launch_ms": fwd_ms,
             "traffic": profiled_traffic(f"fa_fwd_kernel_{args.workload}.md", src),
         }
@@ -534,7 +542,7 @@ def run_fp8(args):
     f = w.fwd_flops()
     value = f / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
-    fp8_peak = 2.0 * peaks["sustained"]  # the nominal fp8 : bf16 dense ratio of the part is 2
+    fp8_peak = 2.0 * peaks["burst"]  # the nominal fp8 : bf16 dense ratio of the part is 2
     print(json.dumps({
         "metric": "attention forward TFLOPs/s, FP8 (e4m3) with incoherent processing, d=128, 1 GB300",
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -544,7 +552,7 @@ def run_fp8(args):
                    "l2": "inputs larger than L2 (no flush between steps)"},
         "roofline": {"bound": "tensor", "kernel": "fa_fwd_fp8 (3 launches)", "achieved": value, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": value / fp8_peak,
-                     "peak_source": peaks["source"] + ", cuBLAS bf16 sustained x 2 (nominal fp8 / bf16 ratio)",
+                     "peak_source": peaks["source"] + ", " + PEAK_NOTE + ", x 2 (nominal fp8 / bf16 ratio)",
                      "traffic": None},
         "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
     return 0
@@ -629,8 +637,9 @@ def run_varlen(args):
            "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
            "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12, "bwd_ms": bwd_ms,
            "roofline": {"bound": "tensor", "kernel": "backward (pre + dK/dV + dQ launches)", "achieved": achieved,
-                        "peak": peaks["sustained"], "unit": "TFLOP/s", "frac": achieved / peaks["sustained"],
-                        "peak_source": peaks["source"] + ", cuBLAS bf16 sustained",
+                        "peak": peaks["burst"], "unit": "TFLOP/s", "frac": achieved / peaks["burst"],
+                        "frac_of_sustained": achieved / peaks["sustained"],
+                        "peak_source": peaks["source"] + ", " + PEAK_NOTE,
                         "flops_per_launch": 3.5 * fwd_f, "launch_ms": bwd_ms, "traffic": None},
            "gpu_launches": 4 * args.steps, "clocks": clocks}
     if not args.no_e2e:
