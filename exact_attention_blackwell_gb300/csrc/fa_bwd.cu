@@ -718,7 +718,21 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
 template <int D>
 struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kStages = (D == 64) ? 14 : 7;  // K_j / V_j ring (alternating)
+  static constexpr int kStages = (D == 64) ? 14 : 7;  // ring slots of one tile
+  // K and V have rings of their own (Q is the K ring's first item, dO the V
+  // ring's): a K slot is released when dQ_j completes, a V slot when dP_j does,
+  // so neither load waits on the other's late release.
+  static constexpr int kKSlots = (4 * kStages + 6) / 7;  // 7 -> 4, 14 -> 8
+  static constexpr int kVSlots = kStages - kKSlots;
+  // fill 0 = Q, 1 = dO, 2 + 2 j = K_j, 3 + 2 j = V_j
+  __device__ static int slot(int fill) {
+    const int m = fill >> 1;
+    return (fill & 1) ? kKSlots + m % kVSlots : m % kKSlots;
+  }
+  __device__ static uint32_t phase(int fill) {
+    const int m = fill >> 1;
+    return (uint32_t)(((fill & 1) ? m / kVSlots : m / kKSlots) & 1);
+  }
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8, kLoadWarp = 9;
   // TMEM: S (fp32), dP (fp32; dS bf16 over it once read), dQ (fp32), and the
@@ -799,8 +813,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       // past N); this thread's row, bf16 pairs in memory order, into TMEM as the
       // A operand of the S / dP MMAs.
       uint32_t row[D / 2];
-      const bool got = mbar_wait_warp(bar(C::kBarFull0 + wg), 0, wctx, kBSiteQ);
-      const uint8_t *tile = smem + C::kOffRing + wg * C::kTile;
+      const bool got = mbar_wait_warp(bar(C::kBarFull0 + C::slot(wg)), 0, wctx, kBSiteQ);
+      const uint8_t *tile = smem + C::kOffRing + C::slot(wg) * C::kTile;
 #pragma unroll
       for (int v = 0; v < D / 8; ++v) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
@@ -859,8 +873,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
       const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
-      auto slot_off = [](int fill) { return (uint64_t)(((fill % C::kStages) * C::kTile) >> 4); };
-      auto par = [](int fill) { return (uint32_t)((fill / C::kStages) & 1); };
+      auto slot_off = [](int fill) { return (uint64_t)((C::slot(fill) * C::kTile) >> 4); };
+      auto par = [](int fill) { return C::phase(fill); };
       auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
       // ring fills 0 and 1 held Q and dO; K_j is fill 2 + 2j, V_j fill 3 + 2j
       auto fk = [](int j) { return 2 + 2 * j; };
@@ -881,23 +895,23 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
             mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj(kk), id_s,
                    kk > 0);
           tc_commit(bar(C::kBarDP));
-          tc_commit(bar(C::kBarEmpty0 + fv(j) % C::kStages));  // V_j consumed
+          tc_commit(bar(C::kBarEmpty0 + C::slot(fv(j))));  // V_j consumed
         }
         __syncwarp();
       };
       bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
       // Q and dO are in TMEM: ring slots 0 and 1 may take K/V fills
       if (ok && elect_one()) {
-        mbar_arrive(bar(C::kBarEmpty0 + 0));
-        mbar_arrive(bar(C::kBarEmpty0 + 1));
+        mbar_arrive(bar(C::kBarEmpty0 + C::slot(0)));
+        mbar_arrive(bar(C::kBarEmpty0 + C::slot(1)));
       }
       __syncwarp();
-      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + fk(0) % C::kStages), par(fk(0)), wctx, kBSiteFull);
+      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(0))), par(fk(0)), wctx, kBSiteFull);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         if (lane == 0) FA_LIFE(1, 3);
-        ok = mbar_wait_warp(bar(C::kBarFull0 + fv(0) % C::kStages), par(fv(0)), wctx, kBSiteFull);
+        ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(0))), par(fv(0)), wctx, kBSiteFull);
       }
       if (ok) {
         tc_fence_after();
@@ -909,7 +923,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         if (more) {
           ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
           FA_TRACE_EV(1, j, 12);
-          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + fk(j + 1) % C::kStages), par(fk(j + 1)), wctx, kBSiteFull);
+          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(j + 1))), par(fk(j + 1)), wctx, kBSiteFull);
           if (!ok) break;
           FA_TRACE_EV(1, j, 13);
           tc_fence_after();
@@ -925,11 +939,11 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128),
                    id_dq, (j > 0 || kk > 0));
-          tc_commit(bar(C::kBarEmpty0 + fk(j) % C::kStages));  // K_j consumed
+          tc_commit(bar(C::kBarEmpty0 + C::slot(fk(j))));  // K_j consumed
         }
         __syncwarp();
         if (more) {
-          ok = mbar_wait_warp(bar(C::kBarFull0 + fv(j + 1) % C::kStages), par(fv(j + 1)), wctx, kBSiteFull);
+          ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
           if (!ok) break;
           tc_fence_after();
           issue_dp(j + 1);
@@ -954,17 +968,18 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       // fills 0, 1: Q and dO (fresh slots; the MMA warp releases them once the
       // elementwise warps have copied them into TMEM)
       for (int t = 0; t < 2; ++t) {
-        mbar_arrive_expect_tx(bar(C::kBarFull0 + t), C::kTile);
+        const int st = C::slot(t);
+        mbar_arrive_expect_tx(bar(C::kBarFull0 + st), C::kTile);
         for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_4d_hint(sbase + C::kOffRing + t * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
-                           bar(C::kBarFull0 + t), bx * 64, h, sq.start + q0, sq.bc, once);
+          tma_load_4d_hint(sbase + C::kOffRing + st * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
+                           bar(C::kBarFull0 + st), bx * 64, h, sq.start + q0, sq.bc, once);
       }
       bool ok = true;
       int fill = 2;
       for (int j = 0; j < nb && ok; ++j) {
         for (int kv = 0; kv < 2 && ok; ++kv, ++fill) {
-          const int s = fill % C::kStages;
-          ok = mbar_wait(bar(C::kBarEmpty0 + s), ((fill / C::kStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          const int s = C::slot(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(C::kBarFull0 + s), C::kTile);
           const CUtensorMap *map = kv ? &p.tm_v : &p.tm_k;
@@ -974,8 +989,12 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         }
       }
       const uint64_t t0 = global_timer_ns();
-      for (int f = max(0, fill - C::kStages); f < fill; ++f)
-        while (!mbar_test(bar(C::kBarFull0 + f % C::kStages), (f / C::kStages) & 1) &&
+      // the last issued fill of each slot: the last kKSlots even fills, the last kVSlots odd ones
+      const int ne = (fill + 1) / 2, no = fill / 2;
+      for (int m = max(0, ne - C::kKSlots); m < ne; ++m)
+        while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * m)), C::phase(2 * m)) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      for (int m = max(0, no - C::kVSlots); m < no; ++m)
+        while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * m + 1)), C::phase(2 * m + 1)) &&
                global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   }
