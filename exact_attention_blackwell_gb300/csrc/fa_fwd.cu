@@ -78,17 +78,23 @@ __device__ unsigned long long g_cta_fwd[65536][3];
   } while (0)
 #endif
 
-template <int D>
+template <int D, int QT_ = (D <= 128) ? 2 : 1>
 struct FwdCfg {
-  static constexpr int kQT = (D <= 128) ? 2 : 1;  // query tiles per CTA
-  static constexpr int kStages = (D == 64) ? 6 : (D == 128 ? 4 : 2);
+  static constexpr int kQT = QT_;  // query tiles per CTA
+  // Short form (head dim <= 128, one query tile): half the TMEM and under half
+  // the shared memory, so two CTAs share an SM and one's set-up and epilogue
+  // overlap the other's main loop; the launcher takes it for short sequences
+  // at head dim 64.
+  static constexpr bool kShort = D <= 128 && QT_ == 1;
+  static constexpr int kMinBlocks = kShort ? 2 : 1;
+  static constexpr int kStages = kShort ? (D == 64 ? 5 : 2) : (D == 64) ? 6 : (D == 128 ? 4 : 2);
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile of Q, K, V or O
   static constexpr int kBoxes = D / 64;           // 64-column TMA boxes per tile (16 KB each)
   static constexpr int kThreads = 128 * kQT + 64;
   static constexpr int kMmaWarp = 4 * kQT;
   static constexpr int kLoadWarp = 4 * kQT + 1;
   static constexpr int kOCol = 128 * kQT;  // TMEM column of O_0 (S_t at 128 t)
-  static constexpr int kTmemCols = 512;
+  static constexpr int kTmemCols = kShort ? 256 : 512;
   static_assert(kOCol + kQT * D <= kTmemCols, "TMEM budget");
   // shared memory (offsets from a 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -99,6 +105,7 @@ struct FwdCfg {
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kMinBlocks == 1 || kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 enum WaitSite : int {
@@ -106,9 +113,10 @@ enum WaitSite : int {
   kSiteSFull = 6, kSiteOFull = 7, kSiteDrain = 8
 };
 
-template <int D, bool CAUSAL, int POLY16, bool VARLEN>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+template <int D, bool CAUSAL, int POLY16, bool VARLEN, int QT_>
+__global__ void __launch_bounds__(FwdCfg<D, QT_>::kThreads, FwdCfg<D, QT_>::kMinBlocks)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D, QT_>;
   constexpr int QT = C::kQT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -478,10 +486,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1) fa_fwd_kernel(const __
   if (threadIdx.x == 0) FA_LIFE(6);
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
-int launch_fwd_v(const FwdParams &p_in, cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16, VARLEN>;
+template <int D, bool CAUSAL, bool VARLEN, int QT>
+int launch_fwd_q(const FwdParams &p_in, cudaStream_t stream) {
+  using C = FwdCfg<D, QT>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16, VARLEN, QT>;
   static bool configured = false;  // per process; attribute is per function
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -498,6 +506,23 @@ int launch_fwd_v(const FwdParams &p_in, cudaStream_t stream) {
   p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * D * 2, p.B * p.Hkv) : 1;
   kern<<<(unsigned)n_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Head dim 64, sequences of at most FA_FWD_SHORT_MAX_N_D64 rows (the longest
+// one, for packed batches): the short form, two CTAs per SM.  Measured on
+// GB300 at B*N = 32768, H = 16: +10-17 % at N = 512, +8-14 % at 1024, +5 % at
+// 2048, +1-4 % at 4096 over the two-tile form.  At head dim 128 its two-stage
+// ring is too shallow for the load latency (2-11 % slower), so it is not used.
+#ifndef FA_FWD_SHORT_MAX_N_D64
+#define FA_FWD_SHORT_MAX_N_D64 4096
+#endif
+
+template <int D, bool CAUSAL, bool VARLEN>
+int launch_fwd_v(const FwdParams &p, cudaStream_t stream) {
+  if constexpr (D == 64) {
+    if (p.N <= FA_FWD_SHORT_MAX_N_D64) return launch_fwd_q<D, CAUSAL, VARLEN, 1>(p, stream);
+  }
+  return launch_fwd_q<D, CAUSAL, VARLEN, FwdCfg<D>::kQT>(p, stream);
 }
 
 template <int D, bool CAUSAL>
