@@ -900,7 +900,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
         __syncwarp();
       };
       bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
-      // Q and dO are in TMEM: ring slots 0 and 1 may take K/V fills
+      // Q and dO are in TMEM: their slots (the first of the K ring and of the V ring) may take K/V fills
       if (ok && elect_one()) {
         mbar_arrive(bar(C::kBarEmpty0 + C::slot(0)));
         mbar_arrive(bar(C::kBarEmpty0 + C::slot(1)));
@@ -961,7 +961,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       }
     }
   } else {
-    // ===================================================== TMA producer: Q, dO, then K_j, V_j alternating
+    // ===================================================== TMA producer: Q, dO, then K_j and V_j in turn, each into its own ring
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();  // K, V are re-read by every query tile
       const uint64_t once = policy_evict_first();  // this CTA's Q and dO rows are read once
