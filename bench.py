@@ -362,7 +362,8 @@ def run_ours(args):
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
-           "config": config_of(w), "frac_of_2250_tflops": value / world / NOMINAL_BF16_TFLOPS,
+           "config": dict(config_of(w), input_sha256=inputs.input_sha256(x_cpu)[:16]),
+           "frac_of_2250_tflops": value / world / NOMINAL_BF16_TFLOPS,
            "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms}
     if w.backward:
         dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev)

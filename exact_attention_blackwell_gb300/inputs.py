@@ -20,6 +20,7 @@ Recipe (the pages print no dataset; every workload is synthetic):
 """
 from __future__ import annotations
 
+import hashlib
 import math
 from dataclasses import dataclass, field
 
@@ -173,3 +174,14 @@ def make_packed_inputs(w: PackedWorkload, device="cpu", with_dO: bool = True):
            for n, t in {"q": q, "k": k, "v": v, "dO": dO}.items()}
     out["cu_seqlens"] = torch.tensor(w.cu_seqlens(), dtype=torch.int32, device=device)
     return out
+
+
+def input_sha256(x: dict) -> str:
+    """SHA-256 over the bf16 bits of q, k, v and dO (when present), in that order:
+    the bits the kernels and the oracle both read, logged beside every result."""
+    h = hashlib.sha256()
+    for n in ("q", "k", "v", "dO"):
+        t = x.get(n)
+        if t is not None:
+            h.update(t.detach().contiguous().cpu().view(torch.int16).numpy().tobytes())
+    return h.hexdigest()
