@@ -31,8 +31,11 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *     asynchronous: it validates, enqueues and returns.
  *   - Supported: d in {64, 128, 256}; N >= 1 (any length, ragged tails are
- *     masked); B, H, Hkv >= 1 with H % Hkv == 0; scale finite and > 0; B*H and
- *     B*Hkv below 65536.  Device: compute capability 10.3 (GB300).
+ *     masked); B, H, Hkv >= 1 with H % Hkv == 0; scale finite and > 0; B and H
+ *     at most 65535; B*N*H*d below 2^40 elements (offsets are 64-bit); at most
+ *     2^31 - 1 thread blocks per launch (one per 128 or 256 rows of one (batch,
+ *     head)).  Larger sizes return FA_ERR_UNSUPPORTED.  Device: compute
+ *     capability 10.3 (GB300).
  *   - Outputs must not alias inputs (not checked).
  *   - Errors: every argument check happens before any launch and nothing is
  *     written on error.  A launch failure returns FA_ERR_CUDA.  Faults inside a
