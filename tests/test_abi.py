@@ -59,6 +59,9 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced, calls 
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=65536), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=65536, Hkv=65536), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=65535, H=65535, Hkv=65535, N=4096), fa.FA_ERR_UNSUPPORTED),  # B*N*H*d beyond 2^40
     (dict(q=A + 8), fa.FA_ERR_ALIGNMENT),
     (dict(o=A + 2), fa.FA_ERR_ALIGNMENT),
     (dict(lse=A + 2), fa.FA_ERR_ALIGNMENT),
