@@ -490,12 +490,10 @@ template <int D, bool CAUSAL, bool VARLEN, int QT>
 int launch_fwd_q(const FwdParams &p_in, cudaStream_t stream) {
   using C = FwdCfg<D, QT>;
   auto kern = fa_fwd_kernel<D, CAUSAL, FA_FWD_POLY_PER16, VARLEN, QT>;
-  static bool configured = false;  // per process; attribute is per function
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return FA_ERR_CUDA;
-    configured = true;
-  }
+  // set on every launch: the attribute belongs to the function on the current
+  // device, and a process may drive several devices from several threads
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return FA_ERR_CUDA;
   const int rows_per_cta = 128 * C::kQT;
   const long long n_groups = (p_in.N + rows_per_cta - 1) / rows_per_cta;
   const long long n_ctas = n_groups * p_in.H * p_in.B;
