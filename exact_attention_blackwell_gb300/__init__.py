@@ -174,17 +174,77 @@ def fa_last_device_status(stream=None) -> int:
 
 
 # ------------------------------------------------------------------ torch helpers
+def _check(name, t, dtype, shape):
+    """Raise ValueError unless t has this dtype and shape and is contiguous (the C ABI reads dense
+    memory and cannot tell); returns (name, t) for the device check that follows all of them."""
+    if t is None:
+        raise ValueError(f"{name} is None")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return name, t
+
+
+def _on_cuda(*checked):
+    for name, t in checked:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
 def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, N, H, d] and [B, N, Hkv, d]")
     B, N, H, d = q.shape
     Hkv = k.shape[2]
     return B, N, H, Hkv, d
+
+
+def _check_fixed(q, k, v, o=None, lse=None, dO=None):
+    import torch
+
+    B, N, H, Hkv, d = _dims(q, k)
+    c = [_check("q", q, torch.bfloat16, (B, N, H, d)), _check("k", k, torch.bfloat16, (B, N, Hkv, d)),
+         _check("v", v, torch.bfloat16, (B, N, Hkv, d))]
+    if o is not None:
+        c.append(_check("o", o, torch.bfloat16, (B, N, H, d)))
+    if dO is not None:
+        c.append(_check("dO", dO, torch.bfloat16, (B, N, H, d)))
+    if lse is not None:
+        c.append(_check("lse", lse, torch.float32, (B, H, N)))
+    _on_cuda(*c)
+    return B, N, H, Hkv, d
+
+
+def _check_packed(q, k, v, cu_seqlens, o=None, lse=None, dO=None):
+    import torch
+
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q and k must be [total, H, d] and [total, Hkv, d]")
+    total, H, d = q.shape
+    Hkv = k.shape[1]
+    c = [_check("q", q, torch.bfloat16, (total, H, d)), _check("k", k, torch.bfloat16, (total, Hkv, d)),
+         _check("v", v, torch.bfloat16, (total, Hkv, d))]
+    if cu_seqlens is None or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor of B + 1 offsets")
+    c.append(_check("cu_seqlens", cu_seqlens, torch.int32, (cu_seqlens.numel(),)))
+    if o is not None:
+        c.append(_check("o", o, torch.bfloat16, (total, H, d)))
+    if dO is not None:
+        c.append(_check("dO", dO, torch.bfloat16, (total, H, d)))
+    if lse is not None:
+        c.append(_check("lse", lse, torch.float32, (H, total)))
+    _on_cuda(*c)
+    return total, H, Hkv, d
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     """q [B,N,H,d], k/v [B,N,Hkv,d] bf16 CUDA tensors -> (o bf16, lse fp32 [B,H,N])."""
     import torch
 
-    B, N, H, Hkv, d = _dims(q, k)
+    B, N, H, Hkv, d = _check_fixed(q, k, v, o=out, lse=lse)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -199,7 +259,11 @@ def attention_fwd_fp8(q, k, v, rot_signs=None, scale=None, causal=False, workspa
     +-1 [128] or None -> (o bf16, lse fp32 [B,H,N], workspace holding the e4m3 tensors and scales)."""
     import torch
 
-    B, N, H, Hkv, d = _dims(q, k)
+    if rot_signs is not None:
+        _check("rot_signs", rot_signs, torch.float32, (128,))
+    B, N, H, Hkv, d = _check_fixed(q, k, v)
+    if rot_signs is not None:
+        _on_cuda(("rot_signs", rot_signs))
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     nbytes = fa_fwd_fp8_workspace_bytes(B, H, Hkv, N, d)
     if workspace is None:
@@ -218,8 +282,7 @@ def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=Fal
     CUDA tensor [B+1] -> (o bf16 [total,H,d], lse fp32 [H,total])."""
     import torch
 
-    total, H, d = q.shape
-    Hkv = k.shape[1]
+    total, H, Hkv, d = _check_packed(q, k, v, cu_seqlens, o=out, lse=lse)
     B = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q) if out is None else out
@@ -234,8 +297,7 @@ def attention_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen, scale=None
     """Packed batch backward (layouts of :func:`attention_fwd_varlen`) -> (dq, dk, dv) bf16."""
     import torch
 
-    total, H, d = q.shape
-    Hkv = k.shape[1]
+    total, H, Hkv, d = _check_packed(q, k, v, cu_seqlens, o=o, lse=lse, dO=dO)
     B = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -252,7 +314,7 @@ def attention_bwd(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None,
     """Returns (dq, dk, dv) bf16."""
     import torch
 
-    B, N, H, Hkv, d = _dims(q, k)
+    B, N, H, Hkv, d = _check_fixed(q, k, v, o=o, lse=lse, dO=dO)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     nbytes = fa_bwd_workspace_bytes(B, H, Hkv, N, d)
