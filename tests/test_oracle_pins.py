@@ -27,7 +27,8 @@ def qkv(B, N, H, Hkv, d, seed):
 # ---------------------------------------------------------------- worked example
 @pytest.mark.parametrize("causal", [False, True])
 def test_golden_two_token(oracle_mod, causal):
-    g = json.load(open(os.path.join(GOLDEN, "two_token.json")))
+    with open(os.path.join(GOLDEN, "two_token.json")) as f:
+        g = json.load(f)
     inp = g["inputs"]
     env = {"e": math.e, "log": math.log}
     ev = lambda a: np.array([[eval(x, env) for x in r] for r in a], dtype=np.float64)
