@@ -329,6 +329,8 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
       (k && encode_bf16_tile_map(&p->tm_k, k, mb, mn, Hkv, d, 128)) ||
       (v && encode_bf16_tile_map(&p->tm_v, v, mb, mn, Hkv, d, 128)) ||
       (dO && encode_bf16_tile_map(&p->tm_do, dO, mb, mn, H, d, 128)) ||
+      (q && encode_bf16_tile_map(&p->tm_q64, q, mb, mn, H, d, 64)) ||
+      (dO && encode_bf16_tile_map(&p->tm_do64, dO, mb, mn, H, d, 64)) ||
       (dq && encode_bf16_tile_map(&p->tm_dq, dq, mb, mn, H, d, 128)) ||
       (dk && encode_bf16_tile_map(&p->tm_dk, dk, mb, mn, Hkv, d, 128)) ||
       (dv && encode_bf16_tile_map(&p->tm_dv, dv, mb, mn, Hkv, d, 128)))

@@ -35,6 +35,11 @@
 #define FA_BWD_POLY_PER16 0
 #endif
 
+// dK/dV at head dim 128 on CTA pairs (1, the default) or on single CTAs (0).
+#ifndef FA_DKDV_PAIR
+#define FA_DKDV_PAIR 1
+#endif
+
 namespace fa {
 namespace {
 
@@ -216,11 +221,15 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
 // (fp32) and stored to TMEM as bf16 for the dV MMA.  MASK is a template
 // argument so that unmasked tiles run a branch-free body; the caller picks it
 // uniformly per warp (tcgen05.st is warp-collective), and the masked body zeroes
-// key rows past the sequence and, on the causal diagonal tile (diag), keys after
-// the query.
+// key rows past the sequence and, under the causal mask (diag: the query tile
+// does not lie wholly after the key tile), keys after the query: key row r is
+// hidden from query column qc when qc + qoff < r, qoff = 128 (query tile - key
+// tile), which is 0 on the diagonal tile and -128 on the tile before it (all
+// hidden; a CTA pair's second key tile meets it).
 template <bool MASK, int POLY16 = FA_BWD_POLY_PER16>
 __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[64], const float *lse2_s,
-                                       float scale_log2, int wg, int r, bool row_valid, bool diag, uint32_t p_tm) {
+                                       float scale_log2, int wg, int r, bool row_valid, bool diag, int qoff,
+                                       uint32_t p_tm) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t w[16];
@@ -243,7 +252,7 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[
         }
       }
       if (MASK) {
-        const int qc = 64 * wg + 32 * c + k;  // query column within tile i
+        const int qc = 64 * wg + 32 * c + k + qoff;  // query column within tile i, relative to the key tile
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (!row_valid || (diag && qc + u < r)) pe[32 * c + k + u] = 0.f;
@@ -259,12 +268,22 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[
 // per key row (TMEM lane), warpgroup wg owns query columns [64 wg, 64 wg + 64).
 //   P^T  = 2^(S^T c - LSE2), masked -> registers (fp32) and TMEM over S^T (bf16, dV's A operand)
 //   dS^T = P^T (dP^T - D)            -> TMEM over dP^T (bf16, dK's A operand)
-// C names the barriers, the row ring and the TMEM columns.  Returns false if a wait ran out.
-template <class C, bool CAUSAL>
+// C names the barriers, the row ring and the TMEM columns.  PAIR: the kernel
+// runs as a CTA pair whose rank-0 CTA issues the MMAs; the P and dS signals go
+// to that CTA's barriers and every wait has cluster scope.  Returns false if a
+// wait ran out.
+template <class C, bool CAUSAL, bool PAIR = false>
 __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *smem, uint32_t bar0, uint32_t tmem,
                                           const WaitCtx &wctx, int warp, int n_iter, int i_start, int per_head,
                                           int jt, int kv0, int L) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
+  auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
+    return PAIR ? mbar_wait_warp_cl(b, parity, wctx, site) : mbar_wait_warp(b, parity, wctx, site);
+  };
+  auto signal_mma = [&](int i) {  // the MMA-issuing CTA's barrier i
+    if (PAIR) mbar_arrive_warp_cluster(mapa_shared(bar(i), 0));
+    else mbar_arrive_warp(bar(i));
+  };
   const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
   const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -281,12 +300,13 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
     const float *dlt_s = lse2_s + 128;
     // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
-    ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
+    ok = wait_warp(bar(C::kBarS), it & 1, kBSiteS);
     if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
     tc_fence_after();
-    const bool diag = CAUSAL && i == jt;
+    const bool diag = CAUSAL && i <= jt;
+    const int qoff = 128 * (i - jt);
     const bool need_mask = warp_has_invalid || diag;  // uniform across the warp
     uint32_t sv[2][32];
     tmem_ld_32x32b_x32(s_tm, sv[0]);
@@ -295,15 +315,15 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     reg_tie(sv[1]);
     float pe[64];
     if (need_mask)
-      dkdv_p<true>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, p_tm);
+      dkdv_p<true>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     else
-      dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, p_tm);
+      dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive_warp(bar(C::kBarP));
+    signal_mma(C::kBarP);
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
     // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
-    ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
+    ok = wait_warp(bar(C::kBarDP), it & 1, kBSiteDP);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
     tc_fence_after();
@@ -330,7 +350,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive_warp(bar(C::kBarDS));
+    signal_mma(C::kBarDS);
     mbar_arrive_warp(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
   }
@@ -644,6 +664,297 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   }
   FA_CTA_MARK(0, 2);
   if (threadIdx.x == 0) FA_LIFE(0, 6);
+}
+
+// ================================================================== dK, dV on CTA pairs (head dim 128)
+// The pages put the backward's bottleneck in shared-memory bandwidth and name
+// the tensor cores' CTA-pair mode as its remedy (FA4 paper summary, section
+// 2.C; FA4 article, "Capacidades de Blackwell que lo hicieron posible"): one
+// MMA of M = 256 rows runs on the two SMs of a cluster pair, each holding its
+// own 128 rows of A and half of B, so each SM reads half of every B operand.
+//
+// A cluster of two CTAs shares one 256-row key tile: CTA c (cluster rank c)
+// owns key rows 128c..128c+127 of it (K, V resident, dK, dV, S^T, dP^T in its
+// own TMEM, its own elementwise warps), and the pair walks the query tiles
+// together.  The rank-0 CTA issues every MMA for both:
+//   S^T  = K Q^T,  dP^T = V dO^T   M = 256 keys, N = 128 queries: CTA c
+//                                  supplies query rows 64c..64c+63 (all d)
+//   dV += P^T dO,  dK += dS^T Q     M = 256 keys, N = 128 = d: CTA c supplies
+//                                  head-dim columns 64c..64c+63 (all queries)
+// Each ring slot of Q (or dO) therefore holds, at the same offsets in both CTAs,
+// the CTA's head-dim half for all 128 rows (16 KB, read MN-major by dK/dV) and
+// its 64 query rows in both halves (2 x 8 KB, read K-major by S^T/dP^T).  The
+// MMAs read 2/3 of the shared-memory bytes of the one-CTA kernel per SM.
+// Both CTAs' loads complete on the rank-0 CTA's barriers; its commits arrive
+// on the barriers of both CTAs; the elementwise warps of both signal the rank-0
+// CTA.  Every wait is bounded, and every thread reaches the final cluster
+// barrier, so neither CTA leaves while the other may still use its memory.
+struct DkdvPairCfg : DkdvCfg<128> {
+  static constexpr int kHalfBytes = 64 * 128;    // 64 rows x 64 columns of bf16 (8 KB)
+  static constexpr int kOffRowHalves = 16384;    // in a slot: the MN-major half first, then the row halves
+};
+
+template <bool CAUSAL, bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1) bwd_dkdv_pair_kernel(const __grid_constant__ BwdParams p) {
+  using C = DkdvPairCfg;
+  constexpr int D = 128;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;  // same layout in both CTAs: both return
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+  FA_CTA_MARK(0, 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const int n_kv = (p.N + 127) / 128;
+  const int n_pairs = (n_kv + 1) / 2;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_pairs, p.B * p.Hkv, p.sched_chunk, rank, head);
+  const int jt = 2 * rank + (int)crank;  // this CTA's key tile; causal: pair 0 sees the most query tiles
+  const int kh = head % p.Hkv, b = head / p.Hkv;
+  const int g = p.H / p.Hkv;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;
+  const int Npad = (p.N + 127) / 128 * 128;
+  const int kv0 = jt * 128;
+  if (VARLEN && 256 * rank >= L) return;  // the pair's tile lies past its sequence (both CTAs return)
+  const int n_q = (L + 127) / 128;
+  const int i_start = CAUSAL ? 2 * rank : 0;  // the pair's first key tile decides; the second masks it whole
+  const int per_head = n_q - i_start;
+  const int n_iter = g * per_head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      // P and dS collect one arrival per elementwise warp of both CTAs; the row
+      // ring is local (8 warps); the rest take one arrival (a producer or a commit)
+      const bool pair_warps = i == C::kBarP || i == C::kBarDS;
+      const bool local_warps = i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages;
+      mbar_init(bar(i), pair_warps ? 16u : local_warps ? 8u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_q64);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_do64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    // ===================================================== P^T and dS^T (this CTA's key rows)
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = dkdv_rows<C, CAUSAL, true>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0, L);
+    if (ok) ok = mbar_wait_warp_cl(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
+    const bool has_rows = kv0 < L;                    // the pair's second tile may lie past the end
+    const bool direct = VARLEN && kv0 + 128 > L;      // the next sequence's rows follow: write row by row
+    if (ok && has_rows && direct) {
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
+      acc_to_global<D>(acc_tm, out + ((size_t)(sq.start + kv0 + r) * p.Hkv + kh) * D, 0, mul, kv0 + r < L);
+    } else if (ok && has_rows) {
+      acc_to_smem<D>(acc_tm, stage, r, 0, mul);
+    }
+    fence_proxy_async_smem();
+    if (wg == 0) named_bar_sync(1, 128);
+    else named_bar_sync(2, 128);
+    if (r == 0 && ok && has_rows && !direct) {
+      const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, sq.start + kv0, sq.bc);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    // Same order as the one-CTA kernel: S_0 dP_0 | [P_0] dV_0 S_1 [dS_0] dK_0 dP_1 | ...
+    if (crank == 0) {
+      constexpr uint32_t id_kk = make_idesc_bf16(256, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_dv = make_idesc_bf16(256, D, false, true);     // dV, dK (A in TMEM, B MN-major)
+      const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
+      const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing + C::kOffRowHalves, 0, 1024);  // row halves
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);                 // column half
+      auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
+      auto kmaj_half = [](int kk) { return (uint64_t)(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4); };
+      auto soff = [&](int fill) { return (uint64_t)((C::slot(fill) * C::kTile) >> 4); };
+      auto full_ok = [&](int fill) {
+        return mbar_wait_warp_cl(bar(C::kBarFull0 + C::slot(fill)), C::phase(fill), wctx, kBSiteFull);
+      };
+      auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it)
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_pair(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj_half(kk), id_kk, kk > 0);
+          tc_commit_pair(bar(C::kBarS));
+        }
+        __syncwarp();
+      };
+      auto issue_dp = [&](int it) {  // dP^T = V dO^T   (dO_it is fill 2 it + 1)
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_pair(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj_half(kk), id_kk, kk > 0);
+          tc_commit_pair(bar(C::kBarDP));
+        }
+        __syncwarp();
+      };
+      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      bool ok = mbar_wait_warp_cl(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      if (ok) ok = full_ok(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = full_ok(1);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const bool more = it + 1 < n_iter;
+        FA_TRACE_EV(0, it, 8);
+        ok = mbar_wait_warp_cl(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        if (!ok) break;
+        FA_TRACE_EV(0, it, 9);
+        tc_fence_after();
+        if (elect_one()) {  // dV += P^T dO_it
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColDV, tmem + C::kColS + a_col(kk), ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
+                        id_dv, (it > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
+        }
+        __syncwarp();
+        if (more) {
+          FA_TRACE_EV(0, it, 12);
+          ok = full_ok(2 * it + 2);
+          if (!ok) break;
+          FA_TRACE_EV(0, it, 13);
+          tc_fence_after();
+          issue_s(it + 1);
+        }
+        ok = mbar_wait_warp_cl(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+        if (!ok) break;
+        FA_TRACE_EV(0, it, 10);
+        tc_fence_after();
+        if (elect_one()) {  // dK += dS^T Q_it
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128),
+                        id_dv, (it > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(2 * it)));  // Q_it consumed (S_it, dK_it)
+        }
+        __syncwarp();
+        if (more) {
+          ok = full_ok(2 * it + 3);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
+        FA_TRACE_EV(0, it, 11);
+      }
+      if (elect_one()) {
+        tc_commit_pair(bar(C::kBarFinal));
+        tc_commit_pair(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp_cl(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test_cl(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer (both CTAs; bytes counted by rank 0)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint32_t kv_bar = mapa_shared(bar(C::kBarKV), 0);
+      if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarKV), 2 * 2 * C::kTile);  // K and V of both CTAs
+      for (int bx = 0; bx < D / 64; ++bx) {
+        tma_load_4d_pair(sbase + C::kOffK + bx * 16384, &p.tm_k, kv_bar, bx * 64, kh, sq.start + kv0, sq.bc, keep);
+        tma_load_4d_pair(sbase + C::kOffV + bx * 16384, &p.tm_v, kv_bar, bx * 64, kh, sq.start + kv0, sq.bc, keep);
+      }
+      bool ok = true;
+      int fill = 0, rows_issued = 0;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int hh = kh * g + it / per_head;
+        const int i = i_start + it % per_head;
+        const int row0 = sq.start + i * 128;
+        for (int t = 0; t < 2 && ok; ++t, ++fill) {  // t = 0: Q_it, t = 1: dO_it
+          const int s = C::slot(fill);
+          ok = mbar_wait_cl(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFull0 + s), 2 * C::kTile);  // both CTAs' 32 KB
+          const uint32_t fb = mapa_shared(bar(C::kBarFull0 + s), 0);
+          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+          const CUtensorMap *m128 = t == 0 ? &p.tm_q : &p.tm_do;
+          const CUtensorMap *m64 = t == 0 ? &p.tm_q64 : &p.tm_do64;
+          // this CTA's head-dim half, all 128 rows (MN-major operand of dK / dV)
+          tma_load_4d_pair(dst, m128, fb, 64 * (int)crank, hh, row0, sq.bc, keep);
+          // this CTA's 64 query rows, both halves (K-major operand of S^T / dP^T)
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(dst + C::kOffRowHalves + bx * C::kHalfBytes, m64, fb, bx * 64, hh,
+                             row0 + 64 * (int)crank, sq.bc, keep);
+        }
+        if (!ok) break;
+        const int rs = it % C::kRowStages;
+        ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
+        if (!ok) break;
+        const uint32_t rb = bar(C::kBarRowFull0 + rs);
+        mbar_arrive_expect_tx(rb, 1024);
+        const size_t roff = ((size_t)b * p.H + hh) * Npad + (size_t)i * 128;
+        const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+        bulk_load(rdst, p.lse2 + roff, 512, rb);
+        bulk_load(rdst + 512, p.delta + roff, 512, rb);
+        ++rows_issued;
+      }
+      // drain: rank 0's full barriers count both CTAs' copies; the row ring is local
+      const uint64_t t0 = global_timer_ns();
+      if (crank == 0) {
+        const int nq = (fill + 1) / 2, nd = fill / 2;
+        for (int i = max(0, nq - C::kQSlots); i < nq; ++i)
+          while (!mbar_test_cl(bar(C::kBarFull0 + C::slot(2 * i)), C::phase(2 * i)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        for (int i = max(0, nd - C::kDoSlots); i < nd; ++i)
+          while (!mbar_test_cl(bar(C::kBarFull0 + C::slot(2 * i + 1)), C::phase(2 * i + 1)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_test_cl(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+      for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
+        while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the rank-0 CTA's MMAs and both CTAs' copies are done with both CTAs' memory
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+  FA_CTA_MARK(0, 2);
 }
 
 // Query-row elementwise work of the dQ kernels over all key tiles: one thread
@@ -1520,6 +1831,20 @@ int launch_dkdv_t(const BwdParams &p_in, cudaStream_t stream) {
                              DkdvCfg<D>::kSmemBytes, p, stream);
 }
 
+// Head dim 128: CTA pairs, one per 256-row key tile (a final odd tile pairs
+// with an empty one).
+template <bool CAUSAL>
+int launch_dkdv_pair_t(const BwdParams &p_in, cudaStream_t stream) {
+  const BwdParams p = with_kv_order(p_in, CAUSAL, 128);
+  const long long n_pairs = ((p.N + 127) / 128 + 1) / 2;
+  const unsigned grid = grid_1d(2 * n_pairs, (long long)p.B * p.Hkv);
+  if (!grid) return FA_ERR_UNSUPPORTED;
+  return p.cu_seqlens ? launch_kernel(bwd_dkdv_pair_kernel<CAUSAL, true>, dim3(grid), DkdvPairCfg::kThreads,
+                                      DkdvPairCfg::kSmemBytes, p, stream)
+                      : launch_kernel(bwd_dkdv_pair_kernel<CAUSAL, false>, dim3(grid), DkdvPairCfg::kThreads,
+                                      DkdvPairCfg::kSmemBytes, p, stream);
+}
+
 template <int D, bool CAUSAL>
 int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_q_order(p_in, CAUSAL, D);
@@ -1546,7 +1871,10 @@ int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, con
 int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
   switch (d) {
     case 64: return causal ? launch_dkdv_t<64, true>(p, stream) : launch_dkdv_t<64, false>(p, stream);
-    case 128: return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
+    case 128:
+      if (FA_DKDV_PAIR)
+        return causal ? launch_dkdv_pair_t<true>(p, stream) : launch_dkdv_pair_t<false>(p, stream);
+      return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
     case 256: {
       const BwdParams q = with_kv_order(p, causal, 256);
       const unsigned n = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.Hkv);  // (key tile, head-dim half)

@@ -113,6 +113,85 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx
   return mbar_wait_slow(bar, parity, ctx, site);
 }
 
+// ------------------------------------------------------------------ CTA pairs (clusters of two)
+// The barriers of the kernels that run as CTA pairs (tcgen05 cta_group::2)
+// receive arrivals from the peer CTA's threads (remote arrives through the
+// cluster's shared window), its TMA copies and the leader's tensor-core commits.
+// The data those arrivals publish is TMEM (ordered by the tcgen05 fences around
+// the barrier) and shared memory written by TMA (ordered by the transaction
+// count), so the waits and arrives use the default CTA-scope semantics, the
+// form CTA-pair tensor-core pipelines use.  FA_PAIR_SCOPE_CLUSTER=1 builds them
+// with explicit cluster scope instead: bitwise the same results, but every
+// cluster-scope try_wait made the pair dK/dV kernel 50 % slower on GB300.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address in the cluster's shared window of the same variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Every thread of both CTAs; orders earlier shared-memory work (barrier
+// initialisation, TMEM allocation) before the peer's later accesses.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+#ifndef FA_PAIR_SCOPE_CLUSTER
+#define FA_PAIR_SCOPE_CLUSTER 0
+#endif
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+#if FA_PAIR_SCOPE_CLUSTER
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+#else
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+#endif
+}
+// One arrival per warp on a barrier given by its cluster address (see mbar_arrive_warp).
+__device__ __forceinline__ void mbar_arrive_warp_cluster(uint32_t cluster_addr) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(cluster_addr);
+}
+__device__ __forceinline__ bool mbar_test_cl(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+#if FA_PAIR_SCOPE_CLUSTER
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+#else
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+#endif
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+static __device__ __noinline__ bool mbar_wait_slow_cl(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 128; ++i)
+      if (mbar_test_cl(bar, parity)) return true;
+    if (*ctx.abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ctx.abort = 1;
+      atomicOr(ctx.status, 1u);
+      atomicCAS(ctx.status + 1, 0u, (unsigned)site);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+  if (mbar_test_cl(bar, parity)) return true;
+  return mbar_wait_slow_cl(bar, parity, ctx, site);
+}
+__device__ __forceinline__ bool mbar_wait_warp_cl(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+  bool ok = mbar_test_cl(bar, parity);
+  if (!ok) ok = mbar_wait_slow_cl(bar, parity, ctx, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Whole-warp wait: every lane waits, and the result is made warp-uniform so the
 // .sync.aligned tcgen05 instructions that follow see a converged warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
@@ -141,6 +220,18 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *map, 
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// The CTA-pair form: the copy lands in this CTA's shared memory and completes
+// its bytes on `cluster_bar`, which may be the peer CTA's barrier (the pair's
+// leader counts the bytes both CTAs load for its MMAs).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void *map, uint32_t cluster_bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(cluster_bar), "l"(policy)
       : "memory");
 }
 
@@ -223,6 +314,47 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// CTA-pair forms (cta_group::2).  A kernel uses one cta_group throughout:
+// these allocate, free and commit for both CTAs of the pair, and one MMA of
+// M = 256 rows takes rows 0-127 of A (and writes D rows 0-127) in the CTA of
+// rank 0, rows 128-255 in rank 1; B's N columns are split the same way, the
+// first N/2 from rank 0's shared memory and the rest from rank 1's, at the same
+// shared-memory offsets.  Issued by one thread of the rank-0 CTA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive on the barrier at offset `bar` of both CTAs once the issuing thread's
+// earlier tcgen05 operations complete.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
