@@ -52,8 +52,79 @@ def env_int(k, default):
 
 
 # ------------------------------------------------------------------ clocks
-class ClockSampler:
-    """nvidia-smi sampling of SM clock, power and throttle reasons.
+class NvmlClockSampler:
+    """In-process, read-only NVML sampling of the SM clock and clock-event
+    reasons, every 4 ms on a background thread (the driver's libnvidia-ml is
+    called through ctypes; nothing is set).  Only samples whose host time falls
+    inside the timed window (mark()) are summarised, so even a 0.1 s timed
+    region has its own record."""
+
+    PERIOD_S = 0.004
+    NVML_CLOCK_SM = 1
+    # clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int):
+        import ctypes
+        import threading
+
+        self._ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.handle)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex_v2 failed")
+        self._reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.samples = []
+        self.window = None
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        u = ctypes.c_uint()
+        self.max_mhz = float(u.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, ctypes.c_int(self.NVML_CLOCK_SM), ctypes.byref(u)) == 0 else None
+
+    def _read(self):
+        ct = self._ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, ct.c_int(self.NVML_CLOCK_SM), ct.byref(clk)) != 0:
+            return None
+        reasons = rs.value if self._reasons_fn(self.handle, ct.byref(rs)) == 0 else 0
+        return time.time(), float(clk.value), reasons
+
+    def _run(self):
+        while not self._stop.is_set():
+            s = self._read()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(self.PERIOD_S)
+
+    def start(self):
+        self._thread.start()
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock bounds (time.time()) of the timed region."""
+        self.window = (t0, t1)
+
+    def stop(self):
+        self._stop.set()
+        self._thread.join(timeout=2)
+        inside = [s for s in self.samples if self.window and self.window[0] <= s[0] <= self.window[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples inside the timed region"],
+                    "source": "NVML in-process"}
+        sm = [s[1] for s in inside]
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "samples": len(sm), "window": "timed region", "reasons": reasons,
+                "source": f"NVML in-process, every {self.PERIOD_S * 1e3:.0f} ms"}
+
+
+class SmiClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons (used when
+    the NVML library cannot be loaded).
 
     Sampling starts before the warm-up (nvidia-smi takes a moment to start);
     only the readings whose timestamps fall inside the timed window count.
@@ -118,9 +189,17 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
-                "power_w_median": statistics.median(power), "samples": len(sm),
+                "power_w_median": statistics.median(power), "samples": len(sm), "source": "nvidia-smi -lms 50",
                 "window": "timed region" if used is inside else "whole run (too few samples inside the timed region)",
                 "reasons": sorted(reasons)}
+
+
+def ClockSampler(gpu_index: int):
+    """NVML in-process sampler where the driver library loads, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(gpu_index)
+    except (OSError, AttributeError):
+        return SmiClockSampler(gpu_index)
 
 
 # ------------------------------------------------------------------ peaks and profiles
@@ -487,7 +566,10 @@ def run_ours(args):
         out["cpu_baseline"] = {"value": head_flops(w) / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                                "kind": "oracle", "seconds": t,
                                "sample": f"(batch 0, head 0) slice: {N} query rows x {N} keys, d={d}, "
-                                         f"{'fwd+bwd' if w.backward else 'fwd'}, fp64"}
+                                         f"{'fwd+bwd' if w.backward else 'fwd'}, fp64",
+                               # every (batch, head) slice costs the same: B * H slices make the whole step
+                               "full_problem_seconds_extrapolated": t * B * H,
+                               "extrapolation": f"measured slice time x {B * H} (batch, head) slices; not measured"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
