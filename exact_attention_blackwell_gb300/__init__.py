@@ -38,8 +38,11 @@ SIGNATURES = {
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_noalloc_scratch_bytes": (_SZ, []),
     "fa_exp2_poly": (_I, [_P, _P, _LL, _P]),
     "fa_last_device_status": (_I, [_P]),
+    "fa_last_device_status_site": (_I, [_P, _P]),
+    "fa_debug_stall": (_I, [_I]),
     "fa_rescale_count": (_I, [_P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -153,7 +156,9 @@ def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, caus
                                 _ptr(dv), B, H, Hkv, N, d, float(scale), int(bool(causal)), _stream(stream))
 
 
-FA_BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
+def fa_bwd_noalloc_scratch_bytes() -> int:
+    """Size of fa_bwd_noalloc's built-in scratch array, as the library was built."""
+    return int(lib().fa_bwd_noalloc_scratch_bytes())
 
 
 def fa_exp2_poly(x, y, n, stream=None) -> int:

@@ -473,6 +473,9 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
   if (!aligned16(o) || !aligned16(dq) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
   const size_t need = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
   if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;  // problem too large for the built-in scratch
+  // the device check first: on a GPU other than sm_103 the library's kernels
+  // cannot load, and the call must fail as fa_bwd does (FA_ERR_UNSUPPORTED)
+  if ((rc = check_device()) != FA_OK) return rc;
   void *ws = nullptr;
   if ((rc = scratch_address(&ws)) != FA_OK) return rc;
   BwdParams p;
@@ -486,6 +489,8 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
   if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
   return launch_bwd_dq(p, d, causal != 0, s);
 }
+
+size_t fa_bwd_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {
   if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID_ARG;
@@ -502,18 +507,34 @@ int fa_exp2_poly(const float *x, float *y, long long n, void *stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_last_device_status(void *stream) {
+int fa_last_device_status_site(void *stream, int *site) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   unsigned *st = device_status_ptr();
   if (!st) return FA_ERR_CUDA;
   unsigned h[2] = {0, 0};
   if (cudaMemcpy(h, st, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (site) *site = h[0] != 0 ? (int)h[1] : 0;
   if (h[0] != 0) {
     const unsigned zero[2] = {0, 0};
     if (cudaMemcpy(st, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
     return FA_ERR_TIMEOUT;
   }
   return FA_OK;
+}
+
+int fa_last_device_status(void *stream) { return fa_last_device_status_site(stream, nullptr); }
+
+int fa_debug_stall(int mode) {
+#ifdef FA_TEST_STALL
+  if (mode < 0 || mode > 3) return FA_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc != FA_OK) return rc;
+  if ((rc = set_test_stall_fwd(mode)) != FA_OK) return rc;
+  return set_test_stall_bwd(mode);
+#else
+  (void)mode;
+  return FA_ERR_UNSUPPORTED;
+#endif
 }
 
 int fa_rescale_count(void *stream, unsigned *count) {

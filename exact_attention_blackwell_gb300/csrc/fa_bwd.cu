@@ -203,6 +203,8 @@ __device__ __forceinline__ void acc_to_global(uint32_t tm_row, __nv_bfloat16 *ds
   }
 }
 
+FA_STALL_FLAG_DECL
+
 enum BwdSite : int {
   kBSiteKV = 11, kBSiteFull = 12, kBSiteEmpty = 13, kBSiteS = 14, kBSiteDP = 15, kBSiteP = 16, kBSiteDS = 17,
   kBSiteDSFree = 18, kBSiteFinal = 19, kBSiteDrain = 20, kBSiteAlign = 21, kBSiteQ = 22
@@ -320,7 +322,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
       dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     tmem_wait_st();
     tc_fence_before();
-    signal_mma(C::kBarP);
+    if (!(FA_STALL(2) && it == 0)) signal_mma(C::kBarP);
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
     // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
     ok = wait_warp(bar(C::kBarDP), it & 1, kBSiteDP);
@@ -1019,7 +1021,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
     tmem_st_32x32b_x32(ds_tm, w);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive_warp(bar(C::kBarDS));
+    if (!(FA_STALL(3) && j == 0)) mbar_arrive_warp(bar(C::kBarDS));
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
   }
   return ok;
@@ -1916,6 +1918,12 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
     default: return FA_ERR_UNSUPPORTED;
   }
 }
+
+#ifdef FA_TEST_STALL
+int set_test_stall_bwd(int mode) {
+  return cudaMemcpyToSymbol(g_test_stall, &mode, sizeof(int)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+#endif
 
 }  // namespace fa
 

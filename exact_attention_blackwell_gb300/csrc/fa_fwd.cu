@@ -108,6 +108,8 @@ struct FwdCfg {
   static_assert(kMinBlocks == 1 || kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
+FA_STALL_FLAG_DECL
+
 enum WaitSite : int {
   kSiteQ = 1, kSiteKFull = 2, kSiteVFull = 3, kSitePFull = 4, kSiteEmpty = 5,
   kSiteSFull = 6, kSiteOFull = 7, kSiteDrain = 8
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT_>::kThreads, FwdCfg<D, QT_>::kMin
       l_sum += (l0 + l1) + (l2 + l3);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(p_bar(t));
+      if (!(FA_STALL(1) && j == 0 && t == 0)) mbar_arrive_warp(p_bar(t));
       if (r == 0) FA_TRACE_EV(j, 3 + 4 * t);
     }
 
@@ -538,6 +540,12 @@ int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream) {
     default: return FA_ERR_UNSUPPORTED;
   }
 }
+
+#ifdef FA_TEST_STALL
+int set_test_stall_fwd(int mode) {
+  return cudaMemcpyToSymbol(g_test_stall, &mode, sizeof(int)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+#endif
 
 }  // namespace fa
 

@@ -150,6 +150,20 @@ unsigned *device_status_ptr();
 // `box_rows` rows of one head, 128-byte swizzle.  Returns 0 on success.
 int encode_bf16_tile_map(CUtensorMap *map, const void *base, int B, int N, int Hx, int d, int box_rows);
 
+// Test builds only (-DFA_TEST_STALL): block 0 of the chosen kernel skips one
+// barrier arrival (1: the forward's first P, 2: the dK/dV kernels' first P,
+// 3: the dQ kernels' first dS), so that a bounded wait runs out and the kernel
+// unwinds through its abort path.  Each translation unit keeps its own flag.
+#ifdef FA_TEST_STALL
+int set_test_stall_fwd(int mode);
+int set_test_stall_bwd(int mode);
+#define FA_STALL_FLAG_DECL static __device__ int g_test_stall;
+#define FA_STALL(k) (g_test_stall == (k) && blockIdx.x == 0)
+#else
+#define FA_STALL_FLAG_DECL
+#define FA_STALL(k) false
+#endif
+
 int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream);
 // The three launches of the backward pass (fa_bwd runs them in this order).
 int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, const float *lse, cudaStream_t stream);

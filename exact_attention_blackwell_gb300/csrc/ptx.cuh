@@ -85,7 +85,13 @@ __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
 // flag (shared memory) and the library's device status word are set, and the
 // caller unwinds without touching the pipeline again.  Other waits in the same
 // CTA see the abort flag and give up at once.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: orders of magnitude above any real wait
+// 4 s by default: orders of magnitude above any real wait.  A test build sets a
+// short limit (FA_WAIT_LIMIT_NS) to make a wait run out on purpose and check
+// that the kernel unwinds and reports it.
+#ifndef FA_WAIT_LIMIT_NS
+#define FA_WAIT_LIMIT_NS 4000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = FA_WAIT_LIMIT_NS;
 
 struct WaitCtx {
   volatile int *abort;  // shared-memory flag of this CTA

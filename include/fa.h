@@ -179,8 +179,13 @@ int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dO, void 
  *     (different streams, or different host threads, without ordering between
  *     them) race and corrupt each other's results.  Each call re-initialises
  *     what it reads, so the contents a previous call left do not matter.
+ *   - The device address is cached for the life of the process: a device
+ *     reset (cudaDeviceReset, or a reset of the primary context) after the
+ *     first call on that device is not supported.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+/* The size of that array as the library was built (FA_BWD_NOALLOC_SCRATCH_BYTES). */
+size_t fa_bwd_noalloc_scratch_bytes(void);
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
                    const void *dO, void *dq, void *dk, void *dv,
                    int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
@@ -201,6 +206,26 @@ int fa_exp2_poly(const float *x, float *y, long long n, void *stream);
  * in any kernel of this library on the current device ran out since the last
  * call (and clears the flag).  Returns FA_ERR_CUDA if synchronisation fails. */
 int fa_last_device_status(void *stream);
+
+/* The same, and writes to *site (host pointer, may be NULL) the id of the first
+ * wait that ran out since the last call, or 0.  Ids name the wait inside the
+ * kernels, for diagnostics: forward 1-8 (1 Q tile loaded, 2/3 K/V tile loaded,
+ * 4 P stored by the softmax warps, 5 ring slot free, 6 S computed, 7 O final,
+ * 8 MMA drain); backward 11-22 (11 K/V loaded, 12 operand tile loaded, 13 ring
+ * slot free, 14 S computed, 15 dP computed, 16 P stored, 17 dS stored,
+ * 19 final MMA, 20 MMA drain, 21 shared-memory alignment, 22 the dQ kernel's
+ * Q and dO tiles loaded).  Outputs of a call in which a wait ran out are
+ * unspecified. */
+int fa_last_device_status_site(void *stream, int *site);
+
+/* Test aid.  In a library built with -DFA_TEST_STALL (never the default
+ * build), makes block 0 of one kernel skip one barrier arrival on every later
+ * launch until called again with mode 0, so that a bounded wait runs out and
+ * the kernel unwinds through its abort path (1: the forward's first P, 2: the
+ * dK/dV kernels' first P, 3: the dQ kernel's first dS); build such a library
+ * with a short -DFA_WAIT_LIMIT_NS.  Returns FA_ERR_INVALID_ARG for another
+ * mode.  In every other build it does nothing and returns FA_ERR_UNSUPPORTED. */
+int fa_debug_stall(int mode);
 
 /* Debugging aid: how many times a warp of the forward kernels applied the
  * conditional O rescale (FlashAttention-4 paper summary, section 2.B: rescale

@@ -171,3 +171,33 @@ def test_fwd_fp8_rejects_bad_arguments(lib):
     assert call(wsb=nb - 1) == fa.FA_ERR_WORKSPACE
     assert call(ws=A + 16) == fa.FA_ERR_WORKSPACE  # 256-byte alignment
     assert call(signs=A + 2) == fa.FA_ERR_ALIGNMENT
+
+
+def test_noalloc_scratch_size_matches_the_header(lib):
+    with open(HEADER) as f:
+        m = re.search(r"#define\s+FA_BWD_NOALLOC_SCRATCH_BYTES\s+\((\d+)ull\s*<<\s*(\d+)\)", f.read())
+    assert m, "FA_BWD_NOALLOC_SCRATCH_BYTES not found in include/fa.h"
+    assert fa.fa_bwd_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_rejects_bad_arguments_like_fa_bwd(lib):
+    good = (1, 2, 2, 256, 128, 0.1, 1, 0)  # B, H, Hkv, N, d, scale, causal, stream
+    p9 = (A,) * 9
+    assert fa.fa_bwd_noalloc(A, A, A, A, A, A, None, A, A, *good) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_noalloc(*p9, 1, 2, 2, 256, 96, 0.1, 1, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_noalloc(*p9, 1, 3, 2, 256, 128, 0.1, 1, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_noalloc(A, A, A, A, A + 2, A, A, A, A, *good) == fa.FA_ERR_ALIGNMENT
+    assert fa.fa_bwd_noalloc(A, A, A, A, A, A, A + 8, A, A, *good) == fa.FA_ERR_ALIGNMENT
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="valid arguments would launch on the GPU with fake addresses")
+def test_noalloc_fails_like_fa_bwd_without_a_usable_device(lib):
+    # arguments that pass every check: the device check decides, and both entry
+    # points must report the same status (no GPU here: the CUDA error)
+    B, H, Hkv, N, d = 1, 2, 2, 256, 128
+    nb = fa.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
+    ws = 0x100000  # 256-byte aligned
+    ref = fa.fa_bwd(A, A, A, A, A, A, A, A, A, B, H, Hkv, N, d, 0.1, 1, ws, nb, 0)
+    got = fa.fa_bwd_noalloc(A, A, A, A, A, A, A, A, A, B, H, Hkv, N, d, 0.1, 1, 0)
+    assert ref != fa.FA_OK and got == ref
