@@ -34,6 +34,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "fa_bwd_fused_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_bwd_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_prepare": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "fa_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_bwd_dq": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -123,6 +125,17 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, work
     return lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B,
                         H, Hkv, N, d, float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
                         _stream(stream))
+
+
+def fa_bwd_fused_workspace_bytes(B, H, Hkv, N, d) -> int:
+    return int(lib().fa_bwd_fused_workspace_bytes(B, H, Hkv, N, d))
+
+
+def fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace_bytes,
+                 stream=None) -> int:
+    return lib().fa_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, H, Hkv, N, d, float(scale), int(bool(causal)), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream))
 
 
 def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, B, max_seqlen, total, H, Hkv, d, scale, causal,
@@ -312,6 +325,23 @@ def attention_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen, scale=None
                        causal, workspace, nbytes, stream)
     if st != FA_OK:
         raise FaError(st, "fa_bwd_varlen")
+    return dq, dk, dv
+
+
+def attention_bwd_fused(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None):
+    """The fused CTA-pair backward (head dim 128): (dq, dk, dv) bf16, not bitwise reproducible."""
+    import torch
+
+    B, N, H, Hkv, d = _check_fixed(q, k, v, o=o, lse=lse, dO=dO)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa_bwd_fused_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    st = fa_bwd_fused(q, k, v, o, lse, dO, dq, dk, dv, B, H, Hkv, N, d, scale, causal, workspace, workspace.numel(),
+                      stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_fused")
     return dq, dk, dv
 
 

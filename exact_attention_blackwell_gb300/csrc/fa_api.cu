@@ -301,6 +301,14 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d) {
   return 2 * up(rows);
 }
 
+size_t fa_bwd_fused_workspace_bytes(int B, int H, int Hkv, int N, int d) {
+  if (d != 128) return 0;
+  const size_t rows = fa_bwd_workspace_bytes(B, H, Hkv, N, d);
+  if (rows == 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return rows + up((size_t)B * N * H * d * sizeof(float));
+}
+
 }  // extern "C"
 
 namespace {
@@ -406,6 +414,25 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;
   if ((rc = launch_bwd_dkdv(p, d, causal != 0, s)) != FA_OK) return rc;
   return launch_bwd_dq(p, d, causal != 0, s);
+}
+
+int fa_bwd_fused(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                 void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_common(B, H, Hkv, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(o) || misaligned4(lse)) return FA_ERR_ALIGNMENT;
+  if (workspace_bytes < fa_bwd_fused_workspace_bytes(B, H, Hkv, N, d)) return FA_ERR_WORKSPACE;
+  BwdParams p;
+  if ((rc = setup_bwd(&p, q, k, v, dO, dq, dk, dv, B, H, Hkv, N, d, scale, workspace, workspace_bytes)) != FA_OK)
+    return rc;
+  p.dqacc = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + fa_bwd_workspace_bytes(B, H, Hkv, N, d));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = launch_bwd_pre(p, d, o, dO, lse, s)) != FA_OK) return rc;  // also zeroes the dQ accumulator
+  if ((rc = launch_bwd_fused(p, causal != 0, s)) != FA_OK) return rc;
+  return launch_bwd_post(p, d, s);
 }
 
 int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,

@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
                                                       float *__restrict__ delta, int B, int H, int N, int Npad,
-                                                      const int *__restrict__ cu, int total) {
+                                                      const int *__restrict__ cu, int total,
+                                                      float *__restrict__ dqacc) {
   constexpr int L = D / 8;      // lanes per row
   constexpr int RPW = 32 / L;   // rows per warp per iteration
   const int lane = threadIdx.x & 31;
@@ -131,6 +132,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
     const size_t off = (grow * H + h) * D + part * 8;
     va[it] = *reinterpret_cast<const uint4 *>(o + off);
     vg[it] = *reinterpret_cast<const uint4 *>(dO + off);
+    if (dqacc != nullptr) {  // the fused backward accumulates dQ here: start from zero
+      float4 *z = reinterpret_cast<float4 *>(dqacc + off);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int it = 0; it < kPreIters; ++it) {
@@ -207,7 +213,8 @@ FA_STALL_FLAG_DECL
 
 enum BwdSite : int {
   kBSiteKV = 11, kBSiteFull = 12, kBSiteEmpty = 13, kBSiteS = 14, kBSiteDP = 15, kBSiteP = 16, kBSiteDS = 17,
-  kBSiteDSFree = 18, kBSiteFinal = 19, kBSiteDrain = 20, kBSiteAlign = 21, kBSiteQ = 22
+  kBSiteDSFree = 18, kBSiteFinal = 19, kBSiteDrain = 20, kBSiteAlign = 21, kBSiteQ = 22, kBSiteDQ = 23,
+  kBSiteSL = 24, kBSiteDQF = 25
 };
 
 __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
@@ -957,6 +964,489 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1) bwd_dkdv_pai
     tmem_dealloc_pair(tmem, C::kTmemCols);
   }
   FA_CTA_MARK(0, 2);
+}
+
+// ================================================================== fused backward on CTA pairs (head dim 128)
+// The pages' backward (FA4 paper summary, section 2.C): one KV-stationary pass
+// computes dK, dV and dQ; the two CTAs of a pair exchange their halves of dS
+// through distributed shared memory, so that each adds dQ for half of the query
+// rows, summed over the pair's 256 keys, and the fp32 reductions into global
+// memory are halved against a one-CTA kernel.
+//
+// A cluster of two CTAs shares one 256-row key tile as in bwd_dkdv_pair_kernel
+// (same S^T, dP^T, dV, dK MMAs and ring layout), plus per query tile i
+//   dQ_i[64c..64c+63, :] += dS[64c..64c+63, 256 keys] K[256 keys, :]
+// as one M = 128 CTA-pair MMA: CTA c supplies the 64 dS rows of its query half
+// (MN-major: one 128-byte line per key holds its 64 queries) and head-dim
+// columns 64c..64c+63 of all 256 K rows; TMEM receives the 64 rows in 64
+// columns, lanes 0-63 holding head-dim columns 0-63 and lanes 64-127 the rest.
+// Elementwise warpgroup w of either CTA computes dS for query half w of its own
+// key rows and writes those lines into CTA w's dS buffer (its own or the
+// peer's).  The warps then move the dQ partial from TMEM to the fp32
+// accumulator with vector reductions, which makes the result depend on the
+// order of the additions (not bitwise reproducible).
+//
+// TMEM: S^T in columns 0-127 (P^T in bf16 packed into 0-63 once S^T is in
+// registers), the dQ partial in 64-127 once the next S^T is in registers; dP^T
+// in 128-255 (dS^T over it), dV 256-383, dK 384-511.  Shared memory: K, V, the
+// dQ operand K (32 KB each), the dS buffer (32 KB), a three-slot Q/dO ring
+// (two Q slots, one dO slot) and the row terms.
+struct FusedCfg {
+  static constexpr int kTile = 128 * 128 * 2;
+  static constexpr int kHalfBytes = 64 * 128;
+  static constexpr int kOffRowHalves = 16384;
+  static constexpr int kQSlots = 2, kDoSlots = 1, kSlots = kQSlots + kDoSlots;
+  __device__ static int slot(int fill) {  // fill 2 i = Q_i, fill 2 i + 1 = dO_i
+    const int i = fill >> 1;
+    return (fill & 1) ? kQSlots + i % kDoSlots : i % kQSlots;
+  }
+  __device__ static uint32_t phase(int fill) {
+    const int i = fill >> 1;
+    return (uint32_t)(((fill & 1) ? i / kDoSlots : i / kQSlots) & 1);
+  }
+  static constexpr int kRowStages = 2;
+  static constexpr int kThreads = 320;
+  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  static constexpr int kColS = 0, kColDQ = 64, kColDP = 128, kColDV = 256, kColDK = 384, kTmemCols = 512;
+  static constexpr int kOffK = 0, kOffV = kTile, kOffKB = 2 * kTile, kOffDS = 3 * kTile, kOffRing = 4 * kTile;
+  static constexpr int kOffRows = kOffRing + kSlots * kTile;
+  enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
+         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages, kBarDP, kBarDQ, kBarSL,
+         kBarP, kBarDS, kBarDQF, kBarFinal, kBarDrain, kBarWG0, kNumBars = kBarWG0 + 4 };
+  static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// dQ partial of query tile t: TMEM -> fp32 reductions into dqacc.  The thread
+// of TMEM lane r holds query row 64 crank + (r % 64) of the tile and head-dim
+// columns 64 (r / 64) + 32 wg .. + 31.
+__device__ __forceinline__ bool fused_dq_out(const BwdParams &p, uint32_t bar0, uint32_t dq_tm, const WaitCtx &wctx,
+                                             int t, int row0, int hh, int b, int wg, int r, int L, bool signal_free) {
+  using C = FusedCfg;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  if (!mbar_wait_warp(bar(C::kBarDQ), t & 1, wctx, kBSiteDQ)) return false;
+  tc_fence_after();
+  uint32_t v[2][16];
+  tmem_ld_32x32b_x16(dq_tm, v[0]);
+  tmem_ld_32x32b_x16(dq_tm + 16, v[1]);
+  tmem_wait_ld(v[0]);
+  tmem_wait_ld(v[1]);
+  tc_fence_before();
+  if (signal_free) mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarDQF), 0));  // columns 64-127 may take the next S
+  const int q = row0 + (r & 63);
+  if (q < L) {
+    float *dst = p.dqacc + (((size_t)b * p.N + q) * p.H + hh) * 128 + (r >> 6) * 64 + 32 * wg;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int k = 0; k < 16; k += 4)
+        red_add_v4(dst + 16 * c + k, __uint_as_float(v[c][k]), __uint_as_float(v[c][k + 1]),
+                   __uint_as_float(v[c][k + 2]), __uint_as_float(v[c][k + 3]));
+  }
+  return true;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool fused_rows(const BwdParams &p, const uint8_t *smem, uint32_t sbase, uint32_t bar0,
+                                           uint32_t tmem, const WaitCtx &wctx, int warp, uint32_t crank, int n_iter,
+                                           int i_start, int per_head, int jt, int kv0, int L, int b, int kh, int g) {
+  using C = FusedCfg;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  auto signal_mma = [&](int i) { mbar_arrive_warp_cluster(mapa_shared(bar(i), 0)); };
+  const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
+  const int r = threadIdx.x & 127;  // key row == TMEM lane
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;
+  const uint32_t p_tm = tmem + lane_off + C::kColS + 32 * wg;  // P^T packed: wg 0 in 0-31, wg 1 in 32-63
+  const uint32_t dq_tm = tmem + lane_off + C::kColDQ + 32 * wg;
+  const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
+  const uint32_t ds_tm = dp_tm;
+  const bool row_valid = kv0 + r < L;
+  const bool warp_has_invalid = __any_sync(0xffffffffu, !row_valid);
+  // this key's dS line (64 queries of half wg) in CTA wg's dS buffer
+  const int kline = 128 * (int)crank + r;
+  const uint32_t ds_line = sbase + C::kOffDS + (uint32_t)kline * 128u;
+  const bool ds_local = wg == (int)crank;
+  const uint32_t ds_remote = mapa_shared(ds_line, (uint32_t)wg);
+  bool ok = true;
+  for (int it = 0; it < n_iter && ok; ++it) {
+    const int rs = it % C::kRowStages;
+    const int i = i_start + it % per_head;
+    const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
+    const float *dlt_s = lse2_s + 128;
+    // ---- S^T -> registers; P^T (bf16) packed into columns 0-63
+    ok = mbar_wait_warp(bar(C::kBarS), it & 1, wctx, kBSiteS);
+    if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
+    tc_fence_after();
+    uint32_t sv[2][32];
+    tmem_ld_32x32b_x32(s_tm, sv[0]);
+    tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+    tmem_wait_ld(sv[0]);
+    reg_tie(sv[1]);
+    tc_fence_before();
+    signal_mma(C::kBarSL);  // columns 64-127 may take the previous tile's dQ
+    // warps w and w+4 (the same TMEM lanes) both hold their S^T before P^T of
+    // warpgroup 1 overwrites columns 32-63 (a bounded wait, unlike bar.sync)
+    mbar_arrive_warp(bar(C::kBarWG0 + (warp & 3)));
+    ok = mbar_wait_warp(bar(C::kBarWG0 + (warp & 3)), it & 1, wctx, kBSiteS);
+    if (!ok) break;
+    const bool diag = CAUSAL && i <= jt;
+    const int qoff = 128 * (i - jt);
+    float pe[64];
+    if (warp_has_invalid || diag)
+      dkdv_p<true>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
+    else
+      dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
+    tmem_wait_st();
+    tc_fence_before();
+    signal_mma(C::kBarP);
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
+    // ---- the previous tile's dQ partial -> fp32 reductions
+    if (it > 0) {
+      const int t = it - 1;
+      ok = fused_dq_out(p, bar0, dq_tm, wctx, t, (i_start + t % per_head) * 128 + 64 * (int)crank,
+                        kh * g + t / per_head, b, wg, r, L, true);
+      if (!ok) break;
+    }
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
+    // ---- dS^T = P^T (dP^T - D): bf16 into TMEM (dK's A) and as a line of dQ's A
+    ok = mbar_wait_warp(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
+    if (!ok) break;
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 3);
+    tc_fence_after();
+    uint32_t dpv[2][32];
+    tmem_ld_32x32b_x32(dp_tm, dpv[0]);
+    tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
+    tmem_wait_ld(dpv[0]);
+    reg_tie(dpv[1]);
+    uint32_t dsw[32];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + 32 * c + k);
+        float t4[4], ds[4];
+        fadd2(t4[0], t4[1], __uint_as_float(dpv[c][k]), __uint_as_float(dpv[c][k + 1]), -d4.x, -d4.y);
+        fadd2(t4[2], t4[3], __uint_as_float(dpv[c][k + 2]), __uint_as_float(dpv[c][k + 3]), -d4.z, -d4.w);
+        fmul2(ds[0], ds[1], pe[32 * c + k], pe[32 * c + k + 1], t4[0], t4[1]);
+        fmul2(ds[2], ds[3], pe[32 * c + k + 2], pe[32 * c + k + 3], t4[2], t4[3]);
+        dsw[16 * c + (k >> 1)] = pack_bf16x2(ds[0], ds[1]);
+        dsw[16 * c + (k >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+    }
+    tmem_st_32x32b_x16(ds_tm, *reinterpret_cast<const uint32_t(*)[16]>(&dsw[0]));
+    tmem_st_32x32b_x16(ds_tm + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dsw[16]));
+    // 128B-swizzled line: 16-byte chunk j (queries 8j..8j+7) at chunk j ^ (line % 8)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t off = (uint32_t)((j ^ (kline & 7)) * 16);
+      if (ds_local)
+        st_shared_v4(ds_line + off, dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+      else
+        st_cluster_v4(ds_remote + off, dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+    }
+    tmem_wait_st();
+    fence_proxy_async_cluster();  // the lines reach the tensor core's reads of either CTA
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_release_cluster(mapa_shared(bar(C::kBarDS), 0));
+    mbar_arrive_warp(bar(C::kBarRowEmpty0 + rs));
+    if (threadIdx.x == 0) FA_TRACE_EV(0, it, 4);
+  }
+  if (ok && n_iter > 0) {  // the last tile's dQ
+    const int t = n_iter - 1;
+    ok = fused_dq_out(p, bar0, dq_tm, wctx, t, (i_start + t % per_head) * 128 + 64 * (int)crank,
+                      kh * g + t / per_head, b, wg, r, L, false);
+  }
+  return ok;
+}
+
+template <bool CAUSAL>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1) bwd_fused_pair_kernel(const __grid_constant__ BwdParams p) {
+  using C = FusedCfg;
+  constexpr int D = 128;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;  // same layout in both CTAs: both return
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const int n_kv = (p.N + 127) / 128;
+  const int n_pairs = (n_kv + 1) / 2;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_pairs, p.B * p.Hkv, p.sched_chunk, rank, head);
+  const int jt = 2 * rank + (int)crank;
+  const int kh = head % p.Hkv, b = head / p.Hkv;
+  const int g = p.H / p.Hkv;
+  const int L = p.N;
+  const int Npad = (p.N + 127) / 128 * 128;
+  const int kv0 = jt * 128;
+  const int n_q = (L + 127) / 128;
+  const int i_start = CAUSAL ? 2 * rank : 0;
+  const int per_head = n_q - i_start;
+  const int n_iter = g * per_head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const bool pair_warps = i == C::kBarP || i == C::kBarDS || i == C::kBarSL || i == C::kBarDQF;
+      const bool local_warps = i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages;
+      const bool two_warps = i >= C::kBarWG0;
+      mbar_init(bar(i), pair_warps ? 16u : local_warps ? 8u : two_warps ? 2u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_q64);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_do64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    // ===================================================== P^T, dS^T, dS lines, dQ reductions
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = fused_rows<CAUSAL>(p, smem, sbase, bar0, tmem, wctx, warp, crank, n_iter, i_start, per_head, jt, kv0, L,
+                                 b, kh, g);
+    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
+    const bool has_rows = kv0 < L;
+    if (ok && has_rows) acc_to_smem<D>(acc_tm, stage, r, 0, mul);
+    fence_proxy_async_smem();
+    if (wg == 0) named_bar_sync(1, 128);
+    else named_bar_sync(2, 128);
+    if (r == 0 && ok && has_rows) {
+      const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+      for (int bx = 0; bx < D / 64; ++bx) tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, kv0, b);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    // S_0 dP_0 | [P_0] dV_0 [DQF_-1] S_1 [dS_0] dK_0 [SL_1] dQ_0 dP_1 | [P_1] dV_1 [DQF_0] S_2 ...
+    if (crank == 0) {
+      constexpr uint32_t id_kk = make_idesc_bf16(256, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_dv = make_idesc_bf16(256, D, false, true);     // dV, dK
+      constexpr uint32_t id_dq = make_idesc_bf16(128, D, true, true);      // dQ: A (dS) and B (K) MN-major
+      const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
+      const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
+      const uint64_t kb_d = make_sdesc_sw128(sbase + C::kOffKB, 16384, 1024);
+      const uint64_t ds_d = make_sdesc_sw128(sbase + C::kOffDS, 16384, 1024);
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing + C::kOffRowHalves, 0, 1024);
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
+      auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
+      auto kmaj_half = [](int kk) { return (uint64_t)(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4); };
+      auto soff = [&](int fill) { return (uint64_t)((C::slot(fill) * C::kTile) >> 4); };
+      auto full_ok = [&](int fill) {
+        return mbar_wait_warp(bar(C::kBarFull0 + C::slot(fill)), C::phase(fill), wctx, kBSiteFull);
+      };
+      auto issue_s = [&](int it) {
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_pair(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj_half(kk), id_kk, kk > 0);
+          tc_commit_pair(bar(C::kBarS));
+        }
+        __syncwarp();
+      };
+      auto issue_dp = [&](int it) {
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_pair(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj_half(kk), id_kk, kk > 0);
+          tc_commit_pair(bar(C::kBarDP));
+        }
+        __syncwarp();
+      };
+      auto a_col_ds = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      bool ok = mbar_wait_warp(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      if (ok) ok = full_ok(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = full_ok(1);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const bool more = it + 1 < n_iter;
+        FA_TRACE_EV(0, it, 8);
+        ok = mbar_wait_warp(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        if (!ok) break;
+        FA_TRACE_EV(0, it, 9);
+        tc_fence_after();
+        if (elect_one()) {  // dV += P^T dO_it   (P^T packed in columns 0-63)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColDV, tmem + C::kColS + 8 * kk, ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
+                        id_dv, (it > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(2 * it + 1)));
+        }
+        __syncwarp();
+        if (more) {
+          if (it > 0) ok = mbar_wait_warp(bar(C::kBarDQF), (it - 1) & 1, wctx, kBSiteDQF);  // dQ_{it-1} read out
+          if (ok) ok = full_ok(2 * it + 2);
+          if (!ok) break;
+          FA_TRACE_EV(0, it, 12);
+          tc_fence_after();
+          issue_s(it + 1);
+        }
+        ok = mbar_wait_warp_acq_cluster(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+        if (!ok) break;
+        FA_TRACE_EV(0, it, 10);
+        tc_fence_after();
+        if (elect_one()) {  // dK += dS^T Q_it
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColDK, tmem + C::kColDP + a_col_ds(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128),
+                        id_dv, (it > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(2 * it)));
+        }
+        __syncwarp();
+        if (more) {  // the next S^T is in registers: its columns 64-127 may take dQ_it
+          ok = mbar_wait_warp(bar(C::kBarSL), (it + 1) & 1, wctx, kBSiteSL);
+        } else if (it > 0) {  // no S^T follows (else waited before it): dQ_{it-1} must have been read out
+          ok = mbar_wait_warp(bar(C::kBarDQF), (it - 1) & 1, wctx, kBSiteDQF);
+        }
+        if (!ok) break;
+        FA_TRACE_EV(0, it, 11);
+        tc_fence_after();
+        if (elect_one()) {  // dQ_it = dS K over the pair's 256 keys (16 steps of 16 keys)
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            mma_ss_pair(tmem + C::kColDQ, ds_d + (uint64_t)(kk * 128), kb_d + (uint64_t)(kk * 128), id_dq, kk > 0);
+          tc_commit_pair(bar(C::kBarDQ));
+        }
+        __syncwarp();
+        if (more) {
+          ok = full_ok(2 * it + 3);
+          if (!ok) break;
+          FA_TRACE_EV(0, it, 13);
+          tc_fence_after();
+          issue_dp(it + 1);
+        }
+        FA_TRACE_EV(0, it, 14);
+      }
+      if (elect_one()) {
+        tc_commit_pair(bar(C::kBarFinal));
+        tc_commit_pair(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer (both CTAs; bytes counted by rank 0)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint32_t kv_bar = mapa_shared(bar(C::kBarKV), 0);
+      if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarKV), 2 * 3 * C::kTile);  // K, V, dQ's K operand, both CTAs
+      for (int bx = 0; bx < D / 64; ++bx) {
+        tma_load_4d_pair(sbase + C::kOffK + bx * 16384, &p.tm_k, kv_bar, bx * 64, kh, kv0, b, keep);
+        tma_load_4d_pair(sbase + C::kOffV + bx * 16384, &p.tm_v, kv_bar, bx * 64, kh, kv0, b, keep);
+      }
+      // dQ's B operand: head-dim half crank of both key tiles of the pair
+      for (int t = 0; t < 2; ++t)
+        tma_load_4d_pair(sbase + C::kOffKB + t * 16384, &p.tm_k, kv_bar, 64 * (int)crank, kh, 256 * rank + 128 * t, b,
+                         keep);
+      bool ok = true;
+      int fill = 0, rows_issued = 0;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int hh = kh * g + it / per_head;
+        const int i = i_start + it % per_head;
+        const int row0 = i * 128;
+        for (int t = 0; t < 2 && ok; ++t, ++fill) {
+          const int s = C::slot(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFull0 + s), 2 * C::kTile);
+          const uint32_t fb = mapa_shared(bar(C::kBarFull0 + s), 0);
+          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+          const CUtensorMap *m128 = t == 0 ? &p.tm_q : &p.tm_do;
+          const CUtensorMap *m64 = t == 0 ? &p.tm_q64 : &p.tm_do64;
+          tma_load_4d_pair(dst, m128, fb, 64 * (int)crank, hh, row0, b, keep);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(dst + C::kOffRowHalves + bx * C::kHalfBytes, m64, fb, bx * 64, hh, row0 + 64 * (int)crank,
+                             b, keep);
+        }
+        if (!ok) break;
+        const int rs = it % C::kRowStages;
+        ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
+        if (!ok) break;
+        const uint32_t rb = bar(C::kBarRowFull0 + rs);
+        mbar_arrive_expect_tx(rb, 1024);
+        const size_t roff = ((size_t)b * p.H + hh) * Npad + (size_t)i * 128;
+        const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+        bulk_load(rdst, p.lse2 + roff, 512, rb);
+        bulk_load(rdst + 512, p.delta + roff, 512, rb);
+        ++rows_issued;
+      }
+      const uint64_t t0 = global_timer_ns();
+      if (crank == 0) {
+        const int nq = (fill + 1) / 2, nd = fill / 2;
+        for (int i = max(0, nq - C::kQSlots); i < nq; ++i)
+          while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * i)), C::phase(2 * i)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        for (int i = max(0, nd - C::kDoSlots); i < nd; ++i)
+          while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * i + 1)), C::phase(2 * i + 1)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_test(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+      for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
+        while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
+// dQ = bf16(scale * dQacc), 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__ acc, __nv_bfloat16 *__restrict__ dq,
+                                                       long long n8, float scale) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+    const float4 c = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+    reinterpret_cast<uint4 *>(dq)[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                                                  pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
 }
 
 // Query-row elementwise work of the dQ kernels over all key tiles: one thread
@@ -1794,7 +2284,7 @@ int launch_pre_t(const BwdParams &p, const void *o, const void *dO, const float 
   const long long rows_per_block = 8LL * (32 / (D / 8)) * kPreIters;  // 8 warps
   bwd_pre_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, p.lse2,
-      const_cast<float *>(p.delta), p.B, p.H, p.N, Npad, p.cu_seqlens, p.total);
+      const_cast<float *>(p.delta), p.B, p.H, p.N, Npad, p.cu_seqlens, p.total, p.dqacc);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -1847,6 +2337,15 @@ int launch_dkdv_pair_t(const BwdParams &p_in, cudaStream_t stream) {
                                       DkdvPairCfg::kSmemBytes, p, stream);
 }
 
+template <bool CAUSAL>
+int launch_fused_t(const BwdParams &p_in, cudaStream_t stream) {
+  const BwdParams p = with_kv_order(p_in, CAUSAL, 128);
+  const long long n_pairs = ((p.N + 127) / 128 + 1) / 2;
+  const unsigned grid = grid_1d(2 * n_pairs, (long long)p.B * p.Hkv);
+  if (!grid) return FA_ERR_UNSUPPORTED;
+  return launch_kernel(bwd_fused_pair_kernel<CAUSAL>, dim3(grid), FusedCfg::kThreads, FusedCfg::kSmemBytes, p, stream);
+}
+
 template <int D, bool CAUSAL>
 int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_q_order(p_in, CAUSAL, D);
@@ -1894,6 +2393,23 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
     }
     default: return FA_ERR_UNSUPPORTED;
   }
+}
+
+int launch_bwd_fused(const BwdParams &p, bool causal, cudaStream_t stream) {
+  if (p.dqacc == nullptr || p.cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
+  return causal ? launch_fused_t<true>(p, stream) : launch_fused_t<false>(p, stream);
+}
+
+int launch_bwd_post(const BwdParams &p, int d, cudaStream_t stream) {
+  const long long n8 = (long long)p.B * p.N * p.H * d / 8;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const long long want = (n8 + 255) / 256;
+  const int blocks = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);
+  if (blocks > 0)
+    bwd_post_kernel<<<blocks, 256, 0, stream>>>(p.dqacc, static_cast<__nv_bfloat16 *>(p.dq), n8, p.scale);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {

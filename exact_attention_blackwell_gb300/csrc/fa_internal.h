@@ -63,6 +63,7 @@ struct BwdParams {
   const int *cu_seqlens;  // as in FwdParams
   int total;
   void *dq, *dk, *dv;  // rows of partial varlen tiles are written directly
+  float *dqacc;        // [B, N, H, d] fp32 dQ accumulator of the fused backward (workspace), else nullptr
 };
 
 // Rows of sequence b: the first one's index in the tensor's row dimension, the
@@ -169,5 +170,10 @@ int launch_fwd(const FwdParams &p, int d, bool causal, cudaStream_t stream);
 int launch_bwd_pre(const BwdParams &p, int d, const void *o, const void *dO, const float *lse, cudaStream_t stream);
 int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream);
 int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream);
+// The fused backward on CTA pairs (head dim 128): dK, dV and dQ partials in one
+// kernel, dQ accumulated in p.dqacc (zeroed by launch_bwd_pre when p.dqacc is
+// set), then scaled and rounded to bf16 by launch_bwd_post.
+int launch_bwd_fused(const BwdParams &p, bool causal, cudaStream_t stream);
+int launch_bwd_post(const BwdParams &p, int d, cudaStream_t stream);
 
 }  // namespace fa

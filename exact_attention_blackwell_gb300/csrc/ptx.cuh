@@ -192,6 +192,41 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, Wait
   if (mbar_test_cl(bar, parity)) return true;
   return mbar_wait_slow_cl(bar, parity, ctx, site);
 }
+// Explicit cluster scope, whatever FA_PAIR_SCOPE_CLUSTER says: for a barrier
+// that publishes generic-proxy stores into the other CTA's shared memory
+// (distributed shared memory), which the waiting CTA's MMAs then read.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_test_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+static __device__ __noinline__ bool mbar_wait_slow_acq_cluster(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 128; ++i)
+      if (mbar_test_acq_cluster(bar, parity)) return true;
+    if (*ctx.abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ctx.abort = 1;
+      atomicOr(ctx.status, 1u);
+      atomicCAS(ctx.status + 1, 0u, (unsigned)site);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_warp_acq_cluster(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
+  bool ok = mbar_test_acq_cluster(bar, parity);
+  if (!ok) ok = mbar_wait_slow_acq_cluster(bar, parity, ctx, site);
+  return __all_sync(0xffffffffu, ok);
+}
 __device__ __forceinline__ bool mbar_wait_warp_cl(uint32_t bar, uint32_t parity, WaitCtx ctx, int site) {
   bool ok = mbar_test_cl(bar, parity);
   if (!ok) ok = mbar_wait_slow_cl(bar, parity, ctx, site);
@@ -263,6 +298,26 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 bytes into shared memory: this CTA's (shared::cta address) or, through the
+// cluster window (mapa_shared), the peer CTA's.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// Generic-proxy stores to either CTA's shared memory become visible to the
+// tensor core (async proxy) reads that follow the barrier.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+// Four fp32 added to global memory at a 16-byte aligned address (reduction in L2).
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // L2 eviction-priority policies for cache hints.

@@ -141,6 +141,22 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
                   int B, int max_seqlen, int total, int H, int Hkv, int d, float scale, int causal,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward pass in one fused kernel on CTA pairs (FlashAttention-4 paper
+ * summary, section 2.C: the two CTAs of a pair exchange halves of dS through
+ * distributed shared memory and each adds dQ for half of the query rows), head
+ * dim 128, fixed-length batches.  Same arguments and results as fa_bwd within
+ * the backward tolerance, but dQ is summed over the key tiles by fp32
+ * reductions in global memory, in an order that varies from run to run: the
+ * result is not bitwise reproducible (fa_bwd is).  The workspace
+ * (fa_bwd_fused_workspace_bytes, 256-byte aligned) holds fa_bwd's row terms
+ * followed by an fp32 dQ accumulator of B*N*H*d elements.  Returns
+ * FA_ERR_UNSUPPORTED for a head dim other than 128. */
+size_t fa_bwd_fused_workspace_bytes(int B, int H, int Hkv, int N, int d);
+int fa_bwd_fused(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dO, void *dq, void *dk, void *dv,
+                 int B, int H, int Hkv, int N, int d, float scale, int causal,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* The three launches fa_bwd makes, for callers that schedule them separately
  * (same arguments and rules as fa_bwd; run fa_bwd_prepare first, then the
  * other two in either order, on one stream or ordered streams, with the same
@@ -214,8 +230,9 @@ int fa_last_device_status(void *stream);
  * 8 MMA drain); backward 11-22 (11 K/V loaded, 12 operand tile loaded, 13 ring
  * slot free, 14 S computed, 15 dP computed, 16 P stored, 17 dS stored,
  * 19 final MMA, 20 MMA drain, 21 shared-memory alignment, 22 the dQ kernel's
- * Q and dO tiles loaded).  Outputs of a call in which a wait ran out are
- * unspecified. */
+ * Q and dO tiles loaded; fused backward: 23 dQ partial computed, 24 S read
+ * into registers, 25 dQ partial read out).  Outputs of a call in which a wait
+ * ran out are unspecified. */
 int fa_last_device_status_site(void *stream, int *site);
 
 /* Test aid.  In a library built with -DFA_TEST_STALL (never the default
