@@ -453,7 +453,8 @@ def run_ours(args):
         # executed GEMM flops of each backward kernel: dK/dV recomputes S^T and dP^T
         # (4 GEMMs of 2 N^2 d per head), dQ recomputes S and dP (3 GEMMs)
         gemm = fwd_f / 2  # one N x N x d GEMM pass over all heads, causal halving included
-        kern = ("bwd_dkdv_kernel", dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
+        dkdv_name = "bwd_dkdv_pair_kernel" if d == 128 else "bwd_dkdv_kernel"  # head dim 128 runs on CTA pairs
+        kern = (dkdv_name, dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
             ("bwd_dq_kernel", dq_ms, 3 * gemm, "fa_bwd.cu")
         name, kms, kflops, _ = kern
         src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
