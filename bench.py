@@ -578,6 +578,93 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ one problem split over the ranks
+def run_sharded(args):
+    """--shard: one problem of the workload split over the ranks by (batch, kv head)
+    groups, GQA groups whole, no data-path collective (strong scaling: the total work
+    is fixed as the rank count grows).  Each rank solves its pieces with the same
+    entry points as the default run."""
+    import torch
+
+    import exact_attention_blackwell_gb300 as fa
+    from exact_attention_blackwell_gb300 import inputs, sharding
+
+    world, rank, local = env_int("WORLD_SIZE", 1), env_int("RANK", 0), env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fa.lib()
+    w = workload(args.workload)
+    g = w.H // w.Hkv
+    x = inputs.make_inputs(w, with_dO=w.backward)  # the same problem on every rank
+    dev = torch.device("cuda", local)
+    pieces = []
+    for pc in sharding.head_pieces(w.B, w.Hkv, world, rank):
+        b0, b1, kh0, kh1 = pc
+        t = {n: sharding.slice_piece(x[n], pc, g).to(dev) for n in (("q", "dO") if w.backward else ("q",))}
+        t.update({n: sharding.slice_piece(x[n], pc).to(dev) for n in ("k", "v")})
+        B, H, Hkv = b1 - b0, (kh1 - kh0) * g, kh1 - kh0
+        t["o"] = torch.empty_like(t["q"])
+        t["lse"] = torch.empty((B, H, w.N), dtype=torch.float32, device=dev)
+        if w.backward:
+            t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+            nb = fa.fa_bwd_workspace_bytes(B, H, Hkv, w.N, w.d)
+            t["ws"], t["nb"] = torch.empty(nb, dtype=torch.uint8, device=dev), nb
+        pieces.append((B, H, Hkv, t))
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def step():
+        for B, H, Hkv, t in pieces:
+            st = fa.fa_fwd(t["q"], t["k"], t["v"], t["o"], t["lse"], B, H, Hkv, w.N, w.d, w.sm_scale, w.causal, sptr)
+            if st == fa.FA_OK and w.backward:
+                st = fa.fa_bwd(t["q"], t["k"], t["v"], t["o"], t["lse"], t["dO"], t["dq"], t["dk"], t["dv"], B, H, Hkv,
+                               w.N, w.d, w.sm_scale, w.causal, t["ws"], t["nb"], sptr)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "sharded step")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(wall0, time.time())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = sharding.max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    if fa.fa_last_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    problem_f = w.fwd_flops() + (w.bwd_flops() if w.backward else 0.0)
+    value = problem_f * args.steps / (total_ms * 1e-3) / 1e12  # the whole problem, once per step, over all ranks
+    launches = len(pieces) * (4 if w.backward else 1) * args.steps
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
+            "config": dict(config_of(w), parallelism=f"{w.B * w.Hkv} (batch, kv head) groups split over {world} GPUs"),
+            "gpu_launches_rank0": launches, "pieces_rank0": [list(pc) for pc in sharding.head_pieces(w.B, w.Hkv, world, 0)],
+            "clocks": clocks}), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 # ------------------------------------------------------------------ FP8 forward
 def run_fp8(args):
     """One step = fa_fwd_fp8 (rotation + e4m3 quantization launches + the FP8 forward) on the headline shape."""
@@ -782,6 +869,8 @@ def main():
     ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen", "fp8"], default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shard", action="store_true",
+                    help="split one problem over the ranks by (batch, kv head) groups (strong scaling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases of the same kernels, e.g. for profiling)")
     args = ap.parse_args()
@@ -797,6 +886,8 @@ def main():
         # our arm: about 0.6 s of timed work on the headline workload, long enough for the
         # clock record; the oracle arm: one (batch, head) slice per step, a few seconds each
         args.steps = 20 if args.impl == "reference" else 100
+    if args.shard and args.impl == "ours":
+        return run_sharded(args)
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 

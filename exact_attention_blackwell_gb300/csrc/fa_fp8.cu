@@ -28,6 +28,12 @@
 namespace fa {
 namespace {
 
+// P of the P V product: in TMEM over S's columns (1, the default; the MMA reads
+// its A operand from TMEM) or in a shared-memory tile (0).
+#ifndef FA_FP8_P_TMEM
+#define FA_FP8_P_TMEM 1
+#endif
+
 constexpr int kD = 128;           // head dim of the FP8 path
 constexpr float kE4m3Max = 448.f;
 
@@ -204,6 +210,16 @@ struct Fp8Cfg {
 
 enum Fp8Site : int { kF8Q = 31, kF8K = 32, kF8V = 33, kF8P = 34, kF8Empty = 35, kF8S = 36, kF8O = 37, kF8Drain = 38 };
 
+// A from TMEM (M rows = lanes, four e4m3 per 32-bit column), B from shared memory.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t acc) {
   asm volatile(
@@ -281,7 +297,9 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1) fa_fwd_fp8_kernel(const _
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + 128u * t;
     const uint32_t o_tm = tmem + lane_off + C::kOCol + 128u * t;
+#if !FA_FP8_P_TMEM
     uint8_t *prow = smem + C::kOffP + t * C::kTile + r * 128;  // this row of P_t (128 keys, e4m3, swizzled)
+#endif
     const int q_row = q0[t] + r;
     const size_t kblk = ((size_t)b * p.Hkv + kh) * p.nt;
     // S = (Q8 K8^T) sq sk: the block scales join the softmax scale in one coefficient
@@ -348,9 +366,9 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1) fa_fwd_fp8_kernel(const _
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
       // p = 2^(s coef - m) <= 2^tau, rounded to e4m3 for the P V product; the row
       // sum takes the unrounded p
+      uint32_t pw[32];  // 128 keys, four e4m3 per word, key order
 #pragma unroll
       for (int chunk = 0; chunk < 8; ++chunk) {  // 16 keys per 16-byte chunk
-        uint32_t w[4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int c = 16 * chunk + 4 * q4;
@@ -361,13 +379,24 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1) fa_fwd_fp8_kernel(const _
           for (int u = 0; u < 4; ++u) e[u] = ex2_mufu(x[u]);
           fadd2(l0, l1, l0, l1, e[0], e[1]);
           fadd2(l2, l3, l2, l3, e[2], e[3]);
-          w[q4] = e4m3x4(e[0], e[1], e[2], e[3]);
+          pw[4 * chunk + q4] = e4m3x4(e[0], e[1], e[2], e[3]);
         }
-        *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+#if !FA_FP8_P_TMEM
+        *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) =
+            make_uint4(pw[4 * chunk], pw[4 * chunk + 1], pw[4 * chunk + 2], pw[4 * chunk + 3]);
+#endif
       }
       l_sum += (l0 + l1) + (l2 + l3);
+#if FA_FP8_P_TMEM
+      // P_t over the first 32 of S_t's columns (read already): the A operand of
+      // PV_t,j; S_t,j+1 overwrites them only after PV_t,j (the tensor pipe runs
+      // one thread's MMAs in order)
+      tmem_st_32x32b_x32(s_tm, pw);
+      tmem_wait_st();
+#else
       fence_proxy_async_smem();  // P_t (generic stores) becomes visible to the tensor core
-      tc_fence_before();         // and so do the O rescale's TMEM stores
+#endif
+      tc_fence_before();  // and so do the O rescale's TMEM stores
       mbar_arrive(p_bar(t));
     }
     // ----------------------------------------------------- epilogue: O sv / l -> bf16, row by row
@@ -416,7 +445,11 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1) fa_fwd_fp8_kernel(const _
       const uint64_t vd = ring_desc + (uint64_t)slot * kTileStep;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
+#if FA_FP8_P_TMEM
+        mma_f8_ts(tmem + C::kOCol + 128u * t, tmem + 128u * t + 8u * kk, vd + 2 * kk, idesc, (acc || kk > 0));
+#else
         mma_f8(tmem + C::kOCol + 128u * t, p_desc0 + t * kTileStep + 2 * kk, vd + 2 * kk, idesc, (acc || kk > 0));
+#endif
     };
     bool ok = nb_max > 0;
     if (ok) ok = mbar_wait_warp(q_bar, 0, wctx, kF8Q);
