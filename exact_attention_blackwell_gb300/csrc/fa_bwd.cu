@@ -235,12 +235,12 @@ __device__ __forceinline__ bool check_align(uint32_t sbase, unsigned *status) {
 // hidden from query column qc when qc + qoff < r, qoff = 128 (query tile - key
 // tile), which is 0 on the diagonal tile and -128 on the tile before it (all
 // hidden; a CTA pair's second key tile meets it).
-template <bool MASK, int POLY16 = FA_BWD_POLY_PER16>
-__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[64], const float *lse2_s,
+template <bool MASK, int QW = 64, int POLY16 = FA_BWD_POLY_PER16>
+__device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[QW / 32][32], float (&pe)[QW], const float *lse2_s,
                                        float scale_log2, int wg, int r, bool row_valid, bool diag, int qoff,
                                        uint32_t p_tm) {
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < QW / 32; ++c) {
     uint32_t w[16];
 #pragma unroll
     for (int k = 0; k < 32; k += 4) {
@@ -261,7 +261,7 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[2][32], float (&pe)[
         }
       }
       if (MASK) {
-        const int qc = 64 * wg + 32 * c + k + qoff;  // query column within tile i, relative to the key tile
+        const int qc = QW * wg + 32 * c + k + qoff;  // query column within tile i, relative to the key tile
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           if (!row_valid || (diag && qc + u < r)) pe[32 * c + k + u] = 0.f;
@@ -293,20 +293,22 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     if (PAIR) mbar_arrive_warp_cluster(mapa_shared(bar(i), 0));
     else mbar_arrive_warp(bar(i));
   };
-  const int wg = warp >> 2;         // query columns [64 wg, 64 wg + 64)
-  const int r = threadIdx.x & 127;  // key row within the tile == TMEM lane
+  constexpr int QW = 128 / C::kNumWG;  // query columns per warpgroup
+  constexpr int NC = QW / 32;          // 32-column chunks per thread
+  const int wg = warp >> 2;            // query columns [QW wg, QW wg + QW)
+  const int r = threadIdx.x & 127;     // key row within the tile == TMEM lane
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;  // S^T columns of this warpgroup
-  const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first 32
-  const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
-  const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first 32 dP^T columns
+  const uint32_t s_tm = tmem + lane_off + C::kColS + QW * wg;  // S^T columns of this warpgroup
+  const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first QW / 2
+  const uint32_t dp_tm = tmem + lane_off + C::kColDP + QW * wg;
+  const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first QW / 2 dP^T columns
   const bool row_valid = kv0 + r < L;  // key rows past the sequence: P = 0
   const bool warp_has_invalid = __any_sync(0xffffffffu, !row_valid);
   bool ok = true;
   for (int it = 0; it < n_iter && ok; ++it) {
     const int rs = it % C::kRowStages;
     const int i = i_start + it % per_head;
-    const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + 64 * wg;
+    const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + QW * wg;
     const float *dlt_s = lse2_s + 128;
     // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
     ok = wait_warp(bar(C::kBarS), it & 1, kBSiteS);
@@ -317,16 +319,17 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     const bool diag = CAUSAL && i <= jt;
     const int qoff = 128 * (i - jt);
     const bool need_mask = warp_has_invalid || diag;  // uniform across the warp
-    uint32_t sv[2][32];
-    tmem_ld_32x32b_x32(s_tm, sv[0]);
-    tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+    uint32_t sv[NC][32];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(s_tm + 32 * c, sv[c]);
     tmem_wait_ld(sv[0]);
-    reg_tie(sv[1]);
-    float pe[64];
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_tie(sv[c]);
+    float pe[QW];
     if (need_mask)
-      dkdv_p<true>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
+      dkdv_p<true, QW>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     else
-      dkdv_p<false>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
+      dkdv_p<false, QW>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     tmem_wait_st();
     tc_fence_before();
     if (!(FA_STALL(2) && it == 0)) signal_mma(C::kBarP);
@@ -336,13 +339,14 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
     tc_fence_after();
-    uint32_t dpv[2][32];
-    tmem_ld_32x32b_x32(dp_tm, dpv[0]);
-    tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
-    tmem_wait_ld(dpv[0]);
-    reg_tie(dpv[1]);
+    uint32_t dpv[NC][32];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(dp_tm + 32 * c, dpv[c]);
+    tmem_wait_ld(dpv[0]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_tie(dpv[c]);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
       uint32_t w[16];
 #pragma unroll
       for (int k = 0; k < 32; k += 4) {
@@ -390,8 +394,14 @@ struct DkdvCfg {
     return (uint32_t)(((fill & 1) ? i / kDoSlots : i / kQSlots) & 1);
   }
   static constexpr int kRowStages = 2;  // own full/empty barriers, released after each dS
-  static constexpr int kThreads = 320;
-  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  // Elementwise warpgroups (thread = key row, a warpgroup per 128 / kNumWG query
+  // columns).  Four at head dim 64 (576 threads, 95 registers) halve each
+  // thread's share of the exponentials and dS, but measured 1-4 % slower on
+  // GB300 than two: the iteration is bound by the chain of handoffs between the
+  // MMA and elementwise warps, not by their throughput.
+  static constexpr int kNumWG = 2;
+  static constexpr int kThreads = 32 * (4 * kNumWG + 2);
+  static constexpr int kMmaWarp = 4 * kNumWG, kLoadWarp = 4 * kNumWG + 1;
   static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr int kTmemCols = 512;
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
@@ -409,7 +419,7 @@ struct DkdvCfg {
 };
 
 template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = DkdvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -443,7 +453,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
       const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
-      mbar_init(bar(i), all ? 8u : 1u);  // one arrival per elementwise warp
+      mbar_init(bar(i), all ? (uint32_t)(4 * C::kNumWG) : 1u);  // one arrival per elementwise warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -464,8 +474,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) FA_LIFE(0, 1);
 
-  if (warp < 8) {
-    // ===================================================== P^T and dS^T, one warpgroup per 64 query columns
+  if (warp < 4 * C::kNumWG) {
+    // ===================================================== P^T and dS^T, one warpgroup per 128 / kNumWG query columns
     // P stays in registers (fp32) from its computation to dS; P^T (bf16) goes
     // to TMEM over the S^T columns for the dV MMA, dS^T (bf16) over the dP^T
     // columns once they have been read, for the dK MMA.
@@ -474,7 +484,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0, L);
     // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
-    //      drained once every MMA has completed)
+    //      drained once every MMA has completed); any further warpgroups are done
+    if (wg < 2) {
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     if (threadIdx.x == 0) FA_LIFE(0, 4);
     tc_fence_after();
@@ -498,6 +509,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
       bulk_commit();
       bulk_wait_read_all();
       if (threadIdx.x == 0) FA_LIFE(0, 5);
+    }
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
@@ -538,9 +550,10 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv_kernel(const __grid_constant_
         }
         __syncwarp();
       };
-      // A operand in TMEM: the query columns 64w.. of warpgroup w start at
-      // column 64w of the region; 16 query rows per K step = 8 columns.
-      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      // A operand in TMEM: the QW query columns of warpgroup w start at column
+      // QW w of the region, in bf16 pairs; 16 query rows per K step = 8 columns.
+      constexpr int QW = 128 / C::kNumWG, KPW = QW / 16;  // query columns and 16-row K steps per warpgroup
+      auto a_col = [](int kk) { return (uint32_t)(QW * (kk / KPW) + 8 * (kk % KPW)); };
       bool ok = mbar_wait_warp(bar(C::kBarKV), 0, wctx, kBSiteKV);
       if (ok) ok = full_ok(0);
       if (ok) {
@@ -1457,58 +1470,65 @@ template <class C, bool CAUSAL>
 __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint32_t tmem, const WaitCtx &wctx,
                                         int warp, int nb, int q_row, float lse2, float dlt, int L) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
+  constexpr int KW = 128 / C::kNumWG;  // key columns per warpgroup
+  constexpr int NC = KW / 32;
   const int wg = warp >> 2;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t s_tm = tmem + lane_off + C::kColS + 64 * wg;
-  const uint32_t dp_tm = tmem + lane_off + C::kColDP + 64 * wg;
-  const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first 32 of this warpgroup's dP columns
+  const uint32_t s_tm = tmem + lane_off + C::kColS + KW * wg;
+  const uint32_t dp_tm = tmem + lane_off + C::kColDP + KW * wg;
+  const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first KW / 2 of this warpgroup's dP columns
   bool ok = true;
   for (int j = 0; j < nb && ok; ++j) {
     ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
     tc_fence_after();
-    uint32_t sv[2][32];
-    tmem_ld_32x32b_x32(s_tm, sv[0]);
-    tmem_ld_32x32b_x32(s_tm + 32, sv[1]);
+    uint32_t sv[NC][32];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(s_tm + 32 * c, sv[c]);
     tmem_wait_ld(sv[0]);
-    reg_tie(sv[1]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_tie(sv[c]);
     tc_fence_before();
     mbar_arrive_warp(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
-    const int kvc0 = j * 128 + 64 * wg;                               // first key column of this warpgroup
+    const int kvc0 = j * 128 + KW * wg;                           // first key column of this warpgroup
     const int lim = (CAUSAL ? min(q_row, L - 1) : L - 1) - kvc0;  // last visible column offset
-    float pe[64];
+    float pe[KW];
 #pragma unroll
-    for (int c = 0; c < 64; c += 2) {
+    for (int c = 0; c < KW; c += 2) {
       float x0, x1;
       ffma2(x0, x1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[c >> 5][(c & 31) + 1]), p.scale_log2,
             p.scale_log2, -lse2, -lse2);
       pe[c] = ex2_mufu(x0);
       pe[c + 1] = ex2_mufu(x1);
     }
-    if (lim < 63) {
+    if (lim < KW - 1) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
+      for (int c = 0; c < KW; ++c)
         if (c > lim) pe[c] = 0.f;
     }
     ok = mbar_wait_warp(bar(C::kBarDP), j & 1, wctx, kBSiteDP);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 1);
     tc_fence_after();
-    uint32_t dpv[2][32];
-    tmem_ld_32x32b_x32(dp_tm, dpv[0]);
-    tmem_ld_32x32b_x32(dp_tm + 32, dpv[1]);
-    tmem_wait_ld(dpv[0]);
-    reg_tie(dpv[1]);
-    uint32_t w[32];
+    uint32_t dpv[NC][32];
 #pragma unroll
-    for (int c = 0; c < 64; c += 2) {
+    for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(dp_tm + 32 * c, dpv[c]);
+    tmem_wait_ld(dpv[0]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_tie(dpv[c]);
+    uint32_t w[KW / 2];
+#pragma unroll
+    for (int c = 0; c < KW; c += 2) {
       float t0, t1, d0, d1;
       fadd2(t0, t1, __uint_as_float(dpv[c >> 5][c & 31]), __uint_as_float(dpv[c >> 5][(c & 31) + 1]), -dlt, -dlt);
       fmul2(d0, d1, pe[c], pe[c + 1], t0, t1);
       w[c >> 1] = pack_bf16x2(d0, d1);
     }
-    tmem_st_32x32b_x32(ds_tm, w);
+    if constexpr (KW == 64)
+      tmem_st_32x32b_x32(ds_tm, *reinterpret_cast<const uint32_t(*)[32]>(&w[0]));
+    else
+      tmem_st_32x32b_x16(ds_tm, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
     tmem_wait_st();
     tc_fence_before();
     if (!(FA_STALL(3) && j == 0)) mbar_arrive_warp(bar(C::kBarDS));
@@ -1536,8 +1556,12 @@ struct DqCfg {
     const int m = fill >> 1;
     return (uint32_t)(((fill & 1) ? m / kVSlots : m / kKSlots) & 1);
   }
-  static constexpr int kThreads = 320;
-  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  // Elementwise warpgroups: thread = query row, a warpgroup per 128 / kNumWG
+  // key columns (four at head dim 64 measured 3-4 % slower than two, as for
+  // the dK/dV kernel).
+  static constexpr int kNumWG = 2;
+  static constexpr int kThreads = 32 * (4 * kNumWG + 2);
+  static constexpr int kMmaWarp = 4 * kNumWG, kLoadWarp = 4 * kNumWG + 1;
   // TMEM: S (fp32), dP (fp32; dS bf16 over it once read), dQ (fp32), and the
   // CTA's Q and dO tiles (bf16, two per column) as A operands of the S and dP MMAs.
   static constexpr int kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
@@ -1554,7 +1578,7 @@ struct DqCfg {
 };
 
 template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -1584,7 +1608,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
-      mbar_init(bar(i), (i == C::kBarQdo || i == C::kBarSFree || i == C::kBarDS) ? 8u : 1u);  // per elementwise warp
+      // per elementwise warp: Q and dO come from the first two warpgroups only
+      mbar_init(bar(i), i == C::kBarQdo ? 8u : (i == C::kBarSFree || i == C::kBarDS) ? (uint32_t)(4 * C::kNumWG) : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1605,13 +1630,13 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) FA_LIFE(1, 1);
 
-  if (warp < 8) {
-    // ===================================================== dS = P (dP - D), one warpgroup per 64 key columns
+  if (warp < 4 * C::kNumWG) {
+    // ===================================================== dS = P (dP - D), one warpgroup per 128 / kNumWG key columns
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int q_row = q0 + r;
-    {
+    if (wg < 2) {
       // Q (warpgroup 0) or dO (warpgroup 1): ring fill 0 / 1 (TMA, zero rows
       // past N); this thread's row, bf16 pairs in memory order, into TMEM as the
       // A operand of the S / dP MMAs.
@@ -1642,7 +1667,8 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
     const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
     const float dlt = p.delta[rw];
     bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt, L);
-    // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
+    // ---- epilogue (warpgroups 0 and 1, half the head dim each): dQ * scale -> bf16 -> shared staging -> TMA store
+    if (wg < 2) {
     if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
     if (threadIdx.x == 0) FA_LIFE(1, 4);
     tc_fence_after();
@@ -1663,6 +1689,7 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       bulk_wait_read_all();
       if (threadIdx.x == 0) FA_LIFE(1, 5);
     }
+    }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
     // Order: S_0 dP_0 | [S read] S_{j+1} [dS_j] dQ_j dP_{j+1} | ...
@@ -1678,7 +1705,9 @@ __global__ void __launch_bounds__(320, 1) bwd_dq_kernel(const __grid_constant__ 
       auto kmaj = [](int kk) { return (uint64_t)((((kk >> 2) * 16384 + (kk & 3) * 32)) >> 4); };
       auto slot_off = [](int fill) { return (uint64_t)((C::slot(fill) * C::kTile) >> 4); };
       auto par = [](int fill) { return C::phase(fill); };
-      auto a_col = [](int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); };
+      // dS of warpgroup w (its KW key columns, bf16 pairs) starts at column KW w
+      constexpr int KW = 128 / C::kNumWG, KPW = KW / 16;
+      auto a_col = [](int kk) { return (uint32_t)(KW * (kk / KPW) + 8 * (kk % KPW)); };
       // ring fills 0 and 1 held Q and dO; K_j is fill 2 + 2j, V_j fill 3 + 2j
       auto fk = [](int j) { return 2 + 2 * j; };
       auto fv = [](int j) { return 3 + 2 * j; };
@@ -1830,6 +1859,7 @@ struct Dkdv256Cfg {
   static constexpr int kHalf = kTile / 2;    // 32 KB: 128 rows x 128 columns
   static constexpr int kSlots = 3;
   static constexpr int kRowStages = 2;
+  static constexpr int kNumWG = 2;
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
   static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -2068,6 +2098,7 @@ struct Dq256Cfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kHalf = kTile / 2;
   static constexpr int kSlots = 3;
+  static constexpr int kNumWG = 2;
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
   static constexpr int kColS = 0, kColDP = 128, kColDQ = 256;
