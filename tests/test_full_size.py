@@ -19,12 +19,13 @@ from helpers import check_grad, check_lse, check_o
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def gpu_fwd_bwd(x, w):
+def gpu_fwd_bwd(x, w, fused=False):
     q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
     o, lse = fa.attention_fwd(q, k, v, scale=w.sm_scale, causal=w.causal)
     grads = None
     if w.backward:
-        grads = fa.attention_bwd(q, k, v, o, lse, x["dO"].cuda(), scale=w.sm_scale, causal=w.causal)
+        bwd = fa.attention_bwd_fused if fused else fa.attention_bwd
+        grads = bwd(q, k, v, o, lse, x["dO"].cuda(), scale=w.sm_scale, causal=w.causal)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == fa.FA_OK
     out = {"o": o.cpu(), "lse": lse.cpu()}
@@ -71,6 +72,14 @@ def test_headline_b4_h16_n8192_d128(oracle_mod):
     w = inputs.headline()
     x = inputs.make_inputs(w)
     got = gpu_fwd_bwd(x, w)
+    check_sampled(oracle_mod, w, x, got, groups=[(0, 0), (w.B - 1, w.H - 1)])
+
+
+def test_fused_backward_headline_b4_h16_n8192_d128(oracle_mod):
+    # the CTA-pair fused backward (fa_bwd_fused) on the headline workload
+    w = inputs.headline()
+    x = inputs.make_inputs(w)
+    got = gpu_fwd_bwd(x, w, fused=True)
     check_sampled(oracle_mod, w, x, got, groups=[(0, 0), (w.B - 1, w.H - 1)])
 
 
