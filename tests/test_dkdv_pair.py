@@ -72,7 +72,7 @@ def test_pair_and_single_cta_dkdv_agree_and_match_oracle(oracle_mod, single_cta_
         check_grad(b.cpu(), r, f"single {what} {name}")
         # dQ: the same kernel in both builds; dK, dV: the same MMAs on the same
         # bf16 operands in the same K order, whichever SM holds which rows
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{what} {name}: pair and single CTA differ
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{what} {name}: pair and single CTA differ"
 
 
 @pytest.fixture(scope="module")
