@@ -39,6 +39,10 @@
 #ifndef FA_DKDV_PAIR
 #define FA_DKDV_PAIR 1
 #endif
+// dQ at head dim 128 on CTA pairs (1) or on single CTAs (0, the default).
+#ifndef FA_DQ_PAIR
+#define FA_DQ_PAIR 0
+#endif
 
 namespace fa {
 namespace {
@@ -1468,10 +1472,16 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__
 // per query row (TMEM lane), warpgroup wg owns key columns [64 wg, 64 wg + 64).
 //   P  = 2^(S c - LSE2), masked -> registers (fp32)
 //   dS = P (dP - D)             -> TMEM over dP (bf16, dQ's A operand)
-template <class C, bool CAUSAL>
+// PAIR: the kernel runs as a CTA pair whose rank-0 CTA issues the MMAs; the S
+// and dS signals go to that CTA's barriers.
+template <class C, bool CAUSAL, bool PAIR = false>
 __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint32_t tmem, const WaitCtx &wctx,
                                         int warp, int nb, int q_row, float lse2, float dlt, int L) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
+  auto signal_mma = [&](int i) {  // the MMA-issuing CTA's barrier i
+    if (PAIR) mbar_arrive_warp_cluster(mapa_shared(bar(i), 0));
+    else mbar_arrive_warp(bar(i));
+  };
   constexpr int KW = 128 / C::kNumWG;  // key columns per warpgroup
   constexpr int NC = KW / 32;
   const int wg = warp >> 2;
@@ -1492,7 +1502,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
 #pragma unroll
     for (int c = 1; c < NC; ++c) reg_tie(sv[c]);
     tc_fence_before();
-    mbar_arrive_warp(bar(C::kBarSFree));  // S is in registers: S_{j+1} may overwrite it
+    signal_mma(C::kBarSFree);  // S is in registers: S_{j+1} may overwrite it
     const int kvc0 = j * 128 + KW * wg;                           // first key column of this warpgroup
     const int lim = (CAUSAL ? min(q_row, L - 1) : L - 1) - kvc0;  // last visible column offset
     float pe[KW];
@@ -1533,7 +1543,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
       tmem_st_32x32b_x16(ds_tm, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
     tmem_wait_st();
     tc_fence_before();
-    if (!(FA_STALL(3) && j == 0)) mbar_arrive_warp(bar(C::kBarDS));
+    if (!(FA_STALL(3) && j == 0)) signal_mma(C::kBarDS);
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
   }
   return ok;
@@ -1841,6 +1851,285 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
   }
   FA_CTA_MARK(1, 2);
   if (threadIdx.x == 0) FA_LIFE(1, 6);
+}
+
+// ================================================================== dQ on CTA pairs (head dim 128)
+// The query-stationary counterpart of bwd_dkdv_pair_kernel: a cluster of two
+// CTAs shares one 256-row query tile, CTA c owning query rows 128c..128c+127
+// (its Q and dO in its own TMEM as the A operands, its S, dP and dQ), and the
+// pair walks the key tiles together.  The rank-0 CTA issues every MMA for both:
+//   S = Q K_j^T, dP = dO V_j^T   M = 256 queries, N = 128 keys: CTA c supplies
+//                                key rows 64c..64c+63 of K_j (V_j), all head-dim columns
+//   dQ += dS K_j                 M = 256 queries, N = 128 = d: CTA c supplies
+//                                head-dim columns 64c..64c+63 of all 128 rows of K_j
+// so each SM's MMAs read half of every B operand and each CTA loads 48 KB per
+// key tile instead of 64.  Q and dO arrive by TMA into the first slot of each
+// ring (local barriers), the elementwise warps copy them into TMEM and signal
+// the rank-0 CTA, which then frees those slots in both CTAs.
+struct DqPairCfg : DqCfg<128> {
+  static constexpr int kHalfBytes = 64 * 128;  // 64 rows x 64 columns of bf16
+  static constexpr int kOffRowHalves = 16384;  // in a slot: K's head-dim half, then the 64-row halves
+};
+
+template <bool CAUSAL, bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1) bwd_dq_pair_kernel(const __grid_constant__ BwdParams p) {
+  using C = DqPairCfg;
+  constexpr int D = 128;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;  // same layout in both CTAs: both return
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+  FA_CTA_MARK(1, 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const int n_q = (p.N + 127) / 128;
+  const int n_pairs = (n_q + 1) / 2;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_pairs, p.B * p.H, p.sched_chunk, rank, head);
+  const int pq = CAUSAL ? n_pairs - 1 - rank : rank;  // causal: the longest query rows first
+  const int it_q = 2 * pq + (int)crank;               // this CTA's query tile
+  const int h = head % p.H, b = head / p.H;
+  const int kh = h / (p.H / p.Hkv);
+  const int Npad = n_q * 128;  // row-term arrays are [B, H, Npad]
+  const int q0 = it_q * 128;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;
+  if (VARLEN && 256 * pq >= L) return;  // the pair's tile lies past its sequence (both CTAs return)
+  const int n_kv = (L + 127) / 128;
+  const int nb = CAUSAL ? min(2 * pq + 2, n_kv) : n_kv;  // key tiles the pair's second query tile sees
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i)
+      mbar_init(bar(i), (i == C::kBarQdo || i == C::kBarSFree || i == C::kBarDS) ? 16u : 1u);  // warps of both
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_do);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_k64);
+    prefetch_tmap(&p.tm_v64);
+    prefetch_tmap(&p.tm_dq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    // ===================================================== dS = P (dP - D) for this CTA's query rows
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int q_row = q0 + r;
+    {
+      // Q (warpgroup 0) or dO (warpgroup 1) of this CTA into its TMEM (A operands of S and dP)
+      uint32_t row[D / 2];
+      const bool got = mbar_wait_warp(bar(C::kBarFull0 + C::slot(wg)), 0, wctx, kBSiteQ);
+      const uint8_t *tile = smem + C::kOffRing + C::slot(wg) * C::kTile;
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (got) x = *reinterpret_cast<const uint4 *>(tile + (v >> 3) * 16384 + r * 128 + (((v & 7) ^ (r & 7)) << 4));
+        row[4 * v] = x.x;
+        row[4 * v + 1] = x.y;
+        row[4 * v + 2] = x.z;
+        row[4 * v + 3] = x.w;
+      }
+      const uint32_t dst = tmem + lane_off + (wg == 0 ? C::kColQ : C::kColDO);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&row[32 * c]);
+        tmem_st_32x32b_x32(dst + 32 * c, part);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarQdo), 0));
+    }
+    // rows past the row-term arrays (the pair's second tile past the last one): P = 0
+    const bool in_rows = q_row < Npad;
+    const size_t rw = ((size_t)b * p.H + h) * Npad + (in_rows ? q_row : 0);
+    const float lse2 = in_rows ? p.lse2[rw] : INFINITY;
+    const float dlt = in_rows ? p.delta[rw] : 0.f;
+    bool ok = dq_rows<C, CAUSAL, true>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt, L);
+    // ---- epilogue: dQ * scale -> bf16 -> shared staging -> TMA store
+    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffStage;
+    const bool has_rows = q0 < L;
+    const bool direct = VARLEN && q0 + 128 > L;
+    if (ok && has_rows && direct)
+      acc_to_global<D / 2>(tmem + lane_off + C::kColDQ,
+                           static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)(sq.start + q_row) * p.H + h) * D, wg * (D / 2),
+                           p.scale, q_row < L);
+    else if (ok && has_rows)
+      acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
+    fence_proxy_async_smem();
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 0 && ok && has_rows && !direct) {
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    // Order: S_0 dP_0 | [S read] S_{j+1} [dS_j] dQ_j dP_{j+1} | ...   (as in bwd_dq_kernel)
+    if (crank == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(256, 128, false, false);  // S, dP (A in TMEM, B K-major)
+      constexpr uint32_t id_dq = make_idesc_bf16(256, D, false, true);    // dQ (A = dS in TMEM, B = K MN-major)
+      const uint64_t ring_d = make_sdesc_sw128(sbase + C::kOffRing + C::kOffRowHalves, 0, 1024);  // row halves
+      const uint64_t ring_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);                 // head-dim half
+      auto kmaj_half = [](int kk) { return (uint64_t)(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4); };
+      auto slot_off = [](int fill) { return (uint64_t)((C::slot(fill) * C::kTile) >> 4); };
+      auto par = [](int fill) { return C::phase(fill); };
+      constexpr int KW = 128 / C::kNumWG, KPW = KW / 16;
+      auto a_col = [](int kk) { return (uint32_t)(KW * (kk / KPW) + 8 * (kk % KPW)); };
+      auto fk = [](int j) { return 2 + 2 * j; };
+      auto fv = [](int j) { return 3 + 2 * j; };
+      auto issue_s = [&](int j) {  // S_j = Q K_j^T
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts_pair(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(fk(j)) + kmaj_half(kk), id_s,
+                        kk > 0);
+          tc_commit_pair(bar(C::kBarS));
+        }
+        __syncwarp();
+      };
+      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts_pair(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj_half(kk), id_s,
+                        kk > 0);
+          tc_commit_pair(bar(C::kBarDP));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(fv(j))));  // V_j consumed
+        }
+        __syncwarp();
+      };
+      bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
+      // Q and dO of both CTAs are in TMEM: the first slot of each ring may take K/V fills in both
+      if (ok && elect_one()) {
+        for (int t = 0; t < 2; ++t) {
+          mbar_arrive(bar(C::kBarEmpty0 + C::slot(t)));
+          mbar_arrive_cluster(mapa_shared(bar(C::kBarEmpty0 + C::slot(t)), 1));
+        }
+      }
+      __syncwarp();
+      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(0))), par(fk(0)), wctx, kBSiteFull);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(0))), par(fv(0)), wctx, kBSiteFull);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+      }
+      for (int j = 0; j < nb && ok; ++j) {
+        const bool more = j + 1 < nb;
+        if (more) {
+          ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
+          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(j + 1))), par(fk(j + 1)), wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        ok = mbar_wait_warp(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {  // dQ += dS_j K_j
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128),
+                        id_dq, (j > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarEmpty0 + C::slot(fk(j))));  // K_j consumed
+        }
+        __syncwarp();
+        if (more) {
+          ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(j + 1);
+        }
+      }
+      if (elect_one()) {
+        tc_commit_pair(bar(C::kBarFinal));
+        tc_commit_pair(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer: this CTA's Q and dO (local), then its halves of K_j, V_j
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint64_t once = policy_evict_first();
+      for (int t = 0; t < 2; ++t) {  // fills 0, 1: Q and dO, completed on this CTA's own barriers
+        const int st = C::slot(t);
+        mbar_arrive_expect_tx(bar(C::kBarFull0 + st), C::kTile);
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_4d_hint(sbase + C::kOffRing + st * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
+                           bar(C::kBarFull0 + st), bx * 64, h, sq.start + q0, sq.bc, once);
+      }
+      bool ok = true;
+      int fill = 2;
+      for (int j = 0; j < nb && ok; ++j) {
+        const int row0 = sq.start + j * 128;
+        for (int kv = 0; kv < 2 && ok; ++kv, ++fill) {  // kv = 0: K_j (both parts), kv = 1: V_j (row halves)
+          const int s = C::slot(fill);
+          ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFull0 + s), kv ? 2 * C::kHalfBytes * 2 : 2 * C::kTile);
+          const uint32_t fb = mapa_shared(bar(C::kBarFull0 + s), 0);
+          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+          if (kv == 0)  // K's head-dim half crank, all 128 rows (MN-major operand of dQ)
+            tma_load_4d_pair(dst, &p.tm_k, fb, 64 * (int)crank, kh, row0, sq.bc, keep);
+          for (int bx = 0; bx < 2; ++bx)  // this CTA's 64 key rows, both halves (K-major operand of S / dP)
+            tma_load_4d_pair(dst + C::kOffRowHalves + bx * C::kHalfBytes, kv ? &p.tm_v64 : &p.tm_k64, fb, bx * 64, kh,
+                             row0 + 64 * (int)crank, sq.bc, keep);
+        }
+      }
+      const uint64_t t0 = global_timer_ns();
+      if (crank == 0) {  // rank 0's full barriers count both CTAs' copies
+        const int nk = (fill + 1) / 2, nv = fill / 2;  // fills issued per ring, Q and dO included
+        for (int m = max(0, nk - C::kKSlots); m < nk; ++m)
+          while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * m)), C::phase(2 * m)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        for (int m = max(0, nv - C::kVSlots); m < nv; ++m)
+          while (!mbar_test(bar(C::kBarFull0 + C::slot(2 * m + 1)), C::phase(2 * m + 1)) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+      } else {  // this CTA's own Q and dO copies
+        for (int t = 0; t < 2; ++t)
+          while (!mbar_test(bar(C::kBarFull0 + C::slot(t)), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+  FA_CTA_MARK(1, 2);
 }
 
 // ================================================================== head dim 256
@@ -2379,6 +2668,20 @@ int launch_fused_t(const BwdParams &p_in, cudaStream_t stream) {
   return launch_kernel(bwd_fused_pair_kernel<CAUSAL>, dim3(grid), FusedCfg::kThreads, FusedCfg::kSmemBytes, p, stream);
 }
 
+// Head dim 128: CTA pairs, one per 256-row query tile (a final odd tile pairs
+// with an empty one).
+template <bool CAUSAL>
+int launch_dq_pair_t(const BwdParams &p_in, cudaStream_t stream) {
+  const BwdParams p = with_q_order(p_in, CAUSAL, 128);
+  const long long n_pairs = ((p.N + 127) / 128 + 1) / 2;
+  const unsigned grid = grid_1d(2 * n_pairs, (long long)p.B * p.H);
+  if (!grid) return FA_ERR_UNSUPPORTED;
+  return p.cu_seqlens ? launch_kernel(bwd_dq_pair_kernel<CAUSAL, true>, dim3(grid), DqPairCfg::kThreads,
+                                      DqPairCfg::kSmemBytes, p, stream)
+                      : launch_kernel(bwd_dq_pair_kernel<CAUSAL, false>, dim3(grid), DqPairCfg::kThreads,
+                                      DqPairCfg::kSmemBytes, p, stream);
+}
+
 template <int D, bool CAUSAL>
 int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_q_order(p_in, CAUSAL, D);
@@ -2448,7 +2751,9 @@ int launch_bwd_post(const BwdParams &p, int d, cudaStream_t stream) {
 int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
   switch (d) {
     case 64: return causal ? launch_dq_t<64, true>(p, stream) : launch_dq_t<64, false>(p, stream);
-    case 128: return causal ? launch_dq_t<128, true>(p, stream) : launch_dq_t<128, false>(p, stream);
+    case 128:
+      if (FA_DQ_PAIR) return causal ? launch_dq_pair_t<true>(p, stream) : launch_dq_pair_t<false>(p, stream);
+      return causal ? launch_dq_t<128, true>(p, stream) : launch_dq_t<128, false>(p, stream);
     case 256: {
       const BwdParams q = with_q_order(p, causal, 256);
       const unsigned n = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
