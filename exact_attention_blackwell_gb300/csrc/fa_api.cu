@@ -337,11 +337,13 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
       (k && encode_bf16_tile_map(&p->tm_k, k, mb, mn, Hkv, d, 128)) ||
       (v && encode_bf16_tile_map(&p->tm_v, v, mb, mn, Hkv, d, 128)) ||
       (dO && encode_bf16_tile_map(&p->tm_do, dO, mb, mn, H, d, 128)) ||
-      // 64-row boxes: only the CTA-pair kernels (head dim 128) read them
-      (q && d == 128 && encode_bf16_tile_map(&p->tm_q64, q, mb, mn, H, d, 64)) ||
-      (dO && d == 128 && encode_bf16_tile_map(&p->tm_do64, dO, mb, mn, H, d, 64)) ||
-      (k && d == 128 && encode_bf16_tile_map(&p->tm_k64, k, mb, mn, Hkv, d, 64)) ||
-      (v && d == 128 && encode_bf16_tile_map(&p->tm_v64, v, mb, mn, Hkv, d, 64)) ||
+      // 64-row boxes: only the CTA-pair kernels (head dims 128 and 256) use them
+      (q && d >= 128 && encode_bf16_tile_map(&p->tm_q64, q, mb, mn, H, d, 64)) ||
+      (dO && d >= 128 && encode_bf16_tile_map(&p->tm_do64, dO, mb, mn, H, d, 64)) ||
+      (k && d >= 128 && encode_bf16_tile_map(&p->tm_k64, k, mb, mn, Hkv, d, 64)) ||
+      (v && d >= 128 && encode_bf16_tile_map(&p->tm_v64, v, mb, mn, Hkv, d, 64)) ||
+      (dk && d == 256 && encode_bf16_tile_map(&p->tm_dk64, dk, mb, mn, Hkv, d, 64)) ||
+      (dv && d == 256 && encode_bf16_tile_map(&p->tm_dv64, dv, mb, mn, Hkv, d, 64)) ||
       (dq && encode_bf16_tile_map(&p->tm_dq, dq, mb, mn, H, d, 128)) ||
       (dk && encode_bf16_tile_map(&p->tm_dk, dk, mb, mn, Hkv, d, 128)) ||
       (dv && encode_bf16_tile_map(&p->tm_dv, dv, mb, mn, Hkv, d, 128)))

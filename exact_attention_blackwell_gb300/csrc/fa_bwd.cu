@@ -43,6 +43,11 @@
 #ifndef FA_DQ_PAIR
 #define FA_DQ_PAIR 0
 #endif
+// dK/dV at head dim 256 on CTA pairs of 64 keys each (1, the default) or on
+// one CTA per (key tile, head-dim half) (0).
+#ifndef FA_DKDV256_PAIR
+#define FA_DKDV256_PAIR 1
+#endif
 
 namespace fa {
 namespace {
@@ -2384,6 +2389,477 @@ __global__ void __launch_bounds__(320, 1) bwd_dkdv256_kernel(const __grid_consta
   }
 }
 
+// ================================================================== dK, dV at head dim 256 on CTA pairs
+// Two CTAs of a cluster share one 128-row key tile, 64 keys each, and the
+// rank-0 CTA issues every MMA as an M = 128 `cta_group::2` MMA.  With 64 keys
+// per CTA the accumulators dV, dK (64 x 256 fp32 each) take 128 TMEM columns
+// apiece, so S^T and dP^T are computed once over the whole head dim: no
+// recomputation, unlike the one-CTA kernel above (which splits the head dim).
+//
+// In an M = 128 pair MMA, CTA c supplies rows 0-63 of A and half of B's N, and
+// receives its 64 rows of D with N columns [0, N/2) in TMEM lanes 0-63 and
+// [N/2, N) in lanes 64-127; an A operand in TMEM is read twice, from lanes 0-63
+// for the first half of N and from lanes 64-127 for the second (both measured
+// with a probe on GB300).  So:
+//   S^T  = K Q^T    N = 128 queries: CTA c supplies query rows 64c..64c+63 (all
+//                   of d); A = K from TMEM, copied there once and duplicated in
+//                   both lane halves (128 columns)
+//   dP^T = V dO^T   the same with V from shared memory
+//   dV  += P^T dO   N = 256 = d: CTA c supplies head-dim columns 128c..128c+127
+//   dK  += dS^T Q   (all queries); A = P^T, dS^T from shared memory, written by
+//                   the elementwise warps (lane m holds key m with queries 0-63,
+//                   lane 64+m the same key with queries 64-127)
+// A CTA therefore needs three of the four 64 x 128 quarters of Q_i (and of dO_i):
+// its query half in both head-dim halves, then the other query half in its
+// head-dim half.  The MMAs address both CTAs' shared memory at one offset, and
+// no fixed placement serves both uses, so each stage holds two quarter slots:
+// S^T (dP^T) reads them as loaded, then the slot holding the quarter that only
+// S^T needed is reloaded in place with the quarter that only dK (dV) needs.
+// MMA order per iteration: S_i, dP_i, dV_{i-1}, dK_i, which gives every load and
+// reload about two MMAs of lead with two Q stages and three dO stages; dS^T is
+// computed while dV_{i-1} runs, and P^T is written once dV_{i-1} has read the
+// previous one.
+struct Dkdv256PairCfg {
+  static constexpr int D = 256;
+  static constexpr int kBox = 64 * 128;       // 64 rows x 64 columns of bf16 (one 128B-swizzled TMA box)
+  static constexpr int kQuarter = 2 * kBox;   // 64 rows x 128 columns
+  static constexpr int kStage = 2 * kQuarter;  // two quarter slots
+  static constexpr int kQStages = 2, kDoStages = 3, kRowStages = 2;
+  static constexpr int kThreads = 320;
+  static constexpr int kMmaWarp = 8, kLoadWarp = 9;  // warps 0-7: elementwise (two warpgroups of 32 query columns)
+  static constexpr int kColK = 0, kColS = 128, kColDP = 192, kColDV = 256, kColDK = 384, kTmemCols = 512;
+  static constexpr int kOffV = 0;                                 // 64 keys x 256: 4 boxes
+  static constexpr int kOffP = 4 * kBox;                          // P^T: 64 keys x 128 queries, 2 boxes
+  static constexpr int kOffDS = kOffP + 2 * kBox;                 // dS^T
+  static constexpr int kOffQ = kOffDS + 2 * kBox;                 // Q stages
+  static constexpr int kOffDO = kOffQ + kQStages * kStage;        // dO stages
+  static constexpr int kOffKTmp = kOffDO + 2 * kStage;            // K before its copy into TMEM: dO stage 2
+  static constexpr int kOffRows = kOffDO + kDoStages * kStage;    // LSE2 / D per row stage
+  enum { kBarKV, kBarK, kBarKT, kBarKCopied, kBarFullQ0, kBarEmptyQ0 = kBarFullQ0 + kQStages,
+         kBarReQ0 = kBarEmptyQ0 + kQStages, kBarFullD0 = kBarReQ0 + kQStages, kBarEmptyD0 = kBarFullD0 + kDoStages,
+         kBarReD0 = kBarEmptyD0 + kDoStages, kBarRowFull0 = kBarReD0 + kDoStages,
+         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages, kBarDP, kBarP, kBarDS,
+         kBarVdone, kBarFinal, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// P^T = 2^(S^T c - LSE2) for one key row and 32 query columns (fp32 in pe,
+// packed bf16 pairs in w).  Key row kr (within the pair's 128-key tile) is
+// hidden from query column qc when qc + qoff < kr under the causal mask (diag),
+// qoff = 128 (query tile - key tile); rows past the sequence give 0.
+template <bool MASK>
+__device__ __forceinline__ void dkdv256_p(const uint32_t (&sv)[32], float (&pe)[32], uint32_t (&w)[16],
+                                          const float *lse2_s, float scale_log2, int qc0, int kr, bool row_valid,
+                                          bool diag, int qoff) {
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    const float4 l4 = *reinterpret_cast<const float4 *>(lse2_s + k);
+    float x[4];
+    ffma2(x[0], x[1], __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]), scale_log2, scale_log2, -l4.x, -l4.y);
+    ffma2(x[2], x[3], __uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3]), scale_log2, scale_log2, -l4.z, -l4.w);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pe[k + u] = ex2_mufu(x[u]);
+      if (MASK && (!row_valid || (diag && qc0 + k + u + qoff < kr))) pe[k + u] = 0.f;
+    }
+    w[k >> 1] = pack_bf16x2(pe[k], pe[k + 1]);
+    w[(k >> 1) + 1] = pack_bf16x2(pe[k + 2], pe[k + 3]);
+  }
+}
+
+// 16 packed words (32 columns from col0) of row r into a K-major operand tile
+// of 64-row, 64-column boxes (8 KB each, 128-byte swizzle).
+__device__ __forceinline__ void st_swizzled_32cols_r64(uint32_t tile, int r, int col0, const uint32_t (&w)[16]) {
+  const uint32_t row = tile + (uint32_t)(col0 >> 6) * 8192u + (uint32_t)r * 128u;
+  const int chunk0 = (col0 & 63) >> 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(row + (uint32_t)(((chunk0 + k) ^ (r & 7)) * 16), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+template <bool CAUSAL, bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+    bwd_dkdv256_pair_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dkdv256PairCfg;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;  // same layout in both CTAs: both return
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int crank = (int)cluster_ctarank();
+  const int n_kv = (p.N + 127) / 128;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_kv, p.B * p.Hkv, p.sched_chunk, rank, head);
+  const int jt = rank;  // the pair's key tile; causal: rank 0 sees the most query tiles
+  const int kh = head % p.Hkv, b = head / p.Hkv;
+  const int g = p.H / p.Hkv;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;
+  const int Npad = (p.N + 127) / 128 * 128;
+  const int kv0 = jt * 128;
+  if (VARLEN && kv0 >= L) return;  // the tile lies past its sequence (both CTAs return)
+  const int n_q = (L + 127) / 128;
+  const int i_start = CAUSAL ? jt : 0;
+  const int per_head = n_q - i_start;
+  const int n_iter = g * per_head;
+  const int key0 = kv0 + 64 * crank;  // this CTA's first key row
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      // P, dS and K-in-TMEM collect one arrival per elementwise warp of both CTAs;
+      // the row ring and the K copy are local (8 warps); the rest take one arrival
+      const bool pair_warps = i == C::kBarP || i == C::kBarDS || i == C::kBarKT;
+      const bool local_warps = i == C::kBarKCopied || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
+      mbar_init(bar(i), pair_warps ? 16u : local_warps ? 8u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q64);
+    prefetch_tmap(&p.tm_do64);
+    prefetch_tmap(&p.tm_k64);
+    prefetch_tmap(&p.tm_v64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;  // TMEM lane
+    const int m = r & 63, h = r >> 6;  // key row of this CTA, query half of the S^T / dP^T columns
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    // ---- K -> TMEM (A of S^T): row m in lanes m and 64 + m, head-dim columns 2x, 2x+1 in column x
+    ok = mbar_wait_warp(bar(C::kBarK), 0, wctx, kBSiteKV);
+    if (ok) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int bx = 2 * wg + half;  // 64-column box of K
+        uint32_t kw[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(smem + C::kOffKTmp + bx * C::kBox + m * 128 +
+                                                           ((j ^ (m & 7)) * 16));
+          kw[4 * j] = v.x;
+          kw[4 * j + 1] = v.y;
+          kw[4 * j + 2] = v.z;
+          kw[4 * j + 3] = v.w;
+        }
+        tmem_st_32x32b_x32(tmem + lane_off + C::kColK + 32 * bx, kw);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();  // the region is refilled by TMA (dO stage 2) after this
+    tc_fence_before();
+    mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarKT), 0));
+    mbar_arrive_warp(bar(C::kBarKCopied));
+
+    // ---- P^T and dS^T of this CTA's 64 keys, 32 query columns per thread
+    const uint32_t s_tm = tmem + lane_off + C::kColS + 32 * wg;
+    const uint32_t dp_tm = tmem + lane_off + C::kColDP + 32 * wg;
+    const int kr = 64 * crank + m;  // key row within the pair's tile
+    const bool row_valid = kv0 + kr < L;
+    const bool warp_has_invalid = __any_sync(0xffffffffu, !row_valid);
+    const int qc0 = 64 * h + 32 * wg;  // this thread's first query column
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const int rs = it % C::kRowStages;
+      const int i = i_start + it % per_head;
+      const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + qc0;
+      const float *dlt_s = lse2_s + 128;
+      ok = mbar_wait_warp_cl(bar(C::kBarS), it & 1, wctx, kBSiteS);
+      if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld_32x32b_x32(s_tm, sv);
+      tmem_wait_ld(sv);
+      const bool diag = CAUSAL && i <= jt;
+      const int qoff = 128 * (i - jt);
+      float pe[32];
+      uint32_t wp[16];
+      if (warp_has_invalid || diag)
+        dkdv256_p<true>(sv, pe, wp, lse2_s, p.scale_log2, qc0, kr, row_valid, diag, qoff);
+      else
+        dkdv256_p<false>(sv, pe, wp, lse2_s, p.scale_log2, qc0, kr, row_valid, diag, qoff);
+      // dS^T = P^T (dP^T - D) first: dK_i waits for it while dV_{i-1} runs
+      ok = mbar_wait_warp_cl(bar(C::kBarDP), it & 1, wctx, kBSiteDP);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dpv[32];
+      tmem_ld_32x32b_x32(dp_tm, dpv);
+      tmem_wait_ld(dpv);
+      uint32_t wd[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 d4 = *reinterpret_cast<const float4 *>(dlt_s + k);
+        float t[4], ds[4];
+        fadd2(t[0], t[1], __uint_as_float(dpv[k]), __uint_as_float(dpv[k + 1]), -d4.x, -d4.y);
+        fadd2(t[2], t[3], __uint_as_float(dpv[k + 2]), __uint_as_float(dpv[k + 3]), -d4.z, -d4.w);
+        fmul2(ds[0], ds[1], pe[k], pe[k + 1], t[0], t[1]);
+        fmul2(ds[2], ds[3], pe[k + 2], pe[k + 3], t[2], t[3]);
+        wd[k >> 1] = pack_bf16x2(ds[0], ds[1]);
+        wd[(k >> 1) + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+      // the dS^T buffer is free: dK_{i-1} was issued before dP_i, whose completion was just seen
+      st_swizzled_32cols_r64(sbase + C::kOffDS, m, qc0, wd);
+      fence_proxy_async_smem();
+      tc_fence_before();  // S^T and dP^T have been read: the next S, dP may overwrite them
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarDS), 0));
+      mbar_arrive_warp(bar(C::kBarRowEmpty0 + rs));  // LSE2 / D rows of this stage no longer read
+      // P^T once dV_{i-1} has read the previous one
+      if (it > 0) {
+        ok = mbar_wait_warp_cl(bar(C::kBarVdone), (it - 1) & 1, wctx, kBSiteP);
+        if (!ok) break;
+      }
+      st_swizzled_32cols_r64(sbase + C::kOffP, m, qc0, wp);
+      fence_proxy_async_smem();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarP), 0));
+    }
+    // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 dK * scale (staged in the Q ring)
+    if (ok) ok = mbar_wait_warp_cl(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    const uint32_t stage = sbase + C::kOffQ + wg * 4 * C::kBox;
+    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+    const float mul = wg == 0 ? 1.0f : p.scale;
+    const bool has_rows = key0 < L;
+    const bool direct = VARLEN && key0 + 64 > L;  // the next sequence's rows follow: write row by row
+    if (ok && has_rows && direct) {
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
+      acc_to_global<128>(acc_tm, out + ((size_t)(sq.start + key0 + m) * p.Hkv + kh) * 256 + 128 * h, 0, mul,
+                         key0 + m < L);
+    } else if (ok && has_rows) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(acc_tm + 32 * j, v);
+        tmem_wait_ld(v);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
+        st_swizzled_32cols_r64(stage, m, 128 * h + 32 * j, w);
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + wg, 128);
+    if (r == 0 && ok && has_rows && !direct) {
+      const CUtensorMap *map = wg == 0 ? &p.tm_dv64 : &p.tm_dk64;
+      for (int bx = 0; bx < 4; ++bx) tma_store_4d(map, stage + bx * C::kBox, bx * 64, kh, sq.start + key0, sq.bc);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    if (crank == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S^T (A in TMEM), dP^T
+      constexpr uint32_t id_o = make_idesc_bf16(128, 256, false, true);   // dV, dK (B MN-major)
+      const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
+      const uint64_t p_d = make_sdesc_sw128(sbase + C::kOffP, 0, 1024);
+      const uint64_t ds_d = make_sdesc_sw128(sbase + C::kOffDS, 0, 1024);
+      const uint64_t q_d = make_sdesc_sw128(sbase + C::kOffQ, 0, 1024);
+      const uint64_t q_mn = make_sdesc_sw128(sbase + C::kOffQ, C::kBox, 1024);
+      const uint64_t do_d = make_sdesc_sw128(sbase + C::kOffDO, 0, 1024);
+      const uint64_t do_mn = make_sdesc_sw128(sbase + C::kOffDO, C::kBox, 1024);
+      auto kmaj = [](int kk) { return (uint64_t)(((kk >> 2) * C::kBox + (kk & 3) * 32) >> 4); };
+      auto off = [](int bytes) { return (uint64_t)(bytes >> 4); };
+      bool ok = mbar_wait_warp_cl(bar(C::kBarKV), 0, wctx, kBSiteKV);
+      if (ok) ok = mbar_wait_warp_cl(bar(C::kBarKT), 0, wctx, kBSiteKV);
+      for (int it = 0; it <= n_iter && ok; ++it) {
+        if (it < n_iter) {
+          const int s = it % C::kQStages, sd = it % C::kDoStages;
+          ok = mbar_wait_warp_cl(bar(C::kBarFullQ0 + s), (it / C::kQStages) & 1, wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {  // S^T = K Q^T: head-dim half kk / 8 of this CTA's query rows
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_ts_pair(tmem + C::kColS, tmem + C::kColK + 8 * kk,
+                          q_d + off(s * C::kStage + (kk >> 3) * C::kQuarter) + kmaj(kk & 7), id_s, kk > 0);
+            tc_commit_pair(bar(C::kBarS));
+          }
+          __syncwarp();
+          ok = mbar_wait_warp_cl(bar(C::kBarFullD0 + sd), (it / C::kDoStages) & 1, wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {  // dP^T = V dO^T
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_ss_pair(tmem + C::kColDP, v_d + kmaj(kk),
+                          do_d + off(sd * C::kStage + (kk >> 3) * C::kQuarter) + kmaj(kk & 7), id_s, kk > 0);
+            tc_commit_pair(bar(C::kBarDP));
+          }
+          __syncwarp();
+        }
+        if (it > 0) {  // dV += P^T dO of the previous iteration (its second dO quarter reloaded)
+          const int j = it - 1, sd = j % C::kDoStages;
+          ok = mbar_wait_warp_cl(bar(C::kBarP), j & 1, wctx, kBSiteP);
+          if (ok) ok = mbar_wait_warp_cl(bar(C::kBarReD0 + sd), (j / C::kDoStages) & 1, wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss_pair(tmem + C::kColDV, p_d + kmaj(kk),
+                          do_mn + off(sd * C::kStage + (kk >> 2) * C::kQuarter + (kk & 3) * 2048), id_o,
+                          (j > 0 || kk > 0));
+            tc_commit_pair(bar(C::kBarVdone));
+            tc_commit_pair(bar(C::kBarEmptyD0 + sd));
+          }
+          __syncwarp();
+        }
+        if (it < n_iter) {  // dK += dS^T Q (the second Q quarter reloaded)
+          const int s = it % C::kQStages;
+          ok = mbar_wait_warp_cl(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
+          if (ok) ok = mbar_wait_warp_cl(bar(C::kBarReQ0 + s), (it / C::kQStages) & 1, wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss_pair(tmem + C::kColDK, ds_d + kmaj(kk),
+                          q_mn + off(s * C::kStage + (kk >> 2) * C::kQuarter + (kk & 3) * 2048), id_o,
+                          (it > 0 || kk > 0));
+            tc_commit_pair(bar(C::kBarEmptyQ0 + s));
+          }
+          __syncwarp();
+        }
+      }
+      if (elect_one()) {
+        tc_commit_pair(bar(C::kBarFinal));
+        tc_commit_pair(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp_cl(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test_cl(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer (both CTAs; stage bytes counted by rank 0)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      auto head_of = [&](int it) { return kh * g + it / per_head; };
+      auto row0_of = [&](int it) { return sq.start + (i_start + it % per_head) * 128; };
+      // V on the rank-0 CTA's barrier (both CTAs' MMAs read it); K on this CTA's own (copied into TMEM here)
+      if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarKV), 2 * 4 * C::kBox);
+      mbar_arrive_expect_tx(bar(C::kBarK), 4 * C::kBox);
+      const uint32_t kv_bar = mapa_shared(bar(C::kBarKV), 0);
+      for (int bx = 0; bx < 4; ++bx) {
+        tma_load_4d_pair(sbase + C::kOffV + bx * C::kBox, &p.tm_v64, kv_bar, bx * 64, kh, sq.start + key0, sq.bc,
+                         keep);
+        tma_load_4d(sbase + C::kOffKTmp + bx * C::kBox, &p.tm_k64, bar(C::kBarK), bx * 64, kh, sq.start + key0,
+                    sq.bc);
+      }
+      bool ok = true;
+      int nfq = 0, nrq = 0, nfd = 0, nrd = 0, rows_issued = 0;
+      for (int it = 0; it <= n_iter && ok; ++it) {
+        if (it < n_iter) {  // Q_it: this CTA's query half, both head-dim halves
+          const int s = it % C::kQStages;
+          ok = mbar_wait_cl(bar(C::kBarEmptyQ0 + s), ((it / C::kQStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFullQ0 + s), 2 * C::kStage);
+          const uint32_t fb = mapa_shared(bar(C::kBarFullQ0 + s), 0);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_4d_pair(sbase + C::kOffQ + s * C::kStage + dh * C::kQuarter + bx * C::kBox, &p.tm_q64, fb,
+                               128 * dh + 64 * bx, head_of(it), row0_of(it) + 64 * crank, sq.bc, keep);
+          ++nfq;
+        }
+        if (it > 0) {  // reloads for the previous iteration: the other query half, this CTA's head-dim half
+          const int j = it - 1;
+          ok = mbar_wait_cl(bar(C::kBarS), j & 1, wctx, kBSiteS);  // S^T_j has read the slot
+          if (!ok) break;
+          const int s = j % C::kQStages;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarReQ0 + s), 2 * C::kQuarter);
+          const uint32_t rq = mapa_shared(bar(C::kBarReQ0 + s), 0);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(sbase + C::kOffQ + s * C::kStage + (1 - crank) * C::kQuarter + bx * C::kBox, &p.tm_q64,
+                             rq, 128 * crank + 64 * bx, head_of(j), row0_of(j) + 64 * (1 - crank), sq.bc, keep);
+          ++nrq;
+          ok = mbar_wait_cl(bar(C::kBarDP), j & 1, wctx, kBSiteDP);  // dP^T_j has read the slot
+          if (!ok) break;
+          const int sd = j % C::kDoStages;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarReD0 + sd), 2 * C::kQuarter);
+          const uint32_t rd = mapa_shared(bar(C::kBarReD0 + sd), 0);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(sbase + C::kOffDO + sd * C::kStage + (1 - crank) * C::kQuarter + bx * C::kBox,
+                             &p.tm_do64, rd, 128 * crank + 64 * bx, head_of(j), row0_of(j) + 64 * (1 - crank), sq.bc,
+                             keep);
+          ++nrd;
+        }
+        if (it < n_iter) {  // dO_it, then the row terms
+          const int sd = it % C::kDoStages;
+          if (it == 2) {  // dO stage 2 held the K tile
+            ok = mbar_wait(bar(C::kBarKCopied), 0, wctx, kBSiteKV);
+            if (!ok) break;
+          }
+          ok = mbar_wait_cl(bar(C::kBarEmptyD0 + sd), ((it / C::kDoStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFullD0 + sd), 2 * C::kStage);
+          const uint32_t fb = mapa_shared(bar(C::kBarFullD0 + sd), 0);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_4d_pair(sbase + C::kOffDO + sd * C::kStage + dh * C::kQuarter + bx * C::kBox, &p.tm_do64, fb,
+                               128 * dh + 64 * bx, head_of(it), row0_of(it) + 64 * crank, sq.bc, keep);
+          ++nfd;
+          const int rs = it % C::kRowStages;
+          ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          const uint32_t rb = bar(C::kBarRowFull0 + rs);
+          mbar_arrive_expect_tx(rb, 1024);
+          const size_t roff = ((size_t)b * p.H + head_of(it)) * Npad + (size_t)(i_start + it % per_head) * 128;
+          const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+          bulk_load(rdst, p.lse2 + roff, 512, rb);
+          bulk_load(rdst + 512, p.delta + roff, 512, rb);
+          ++rows_issued;
+        }
+      }
+      // drain: the stage barriers of rank 0 count both CTAs' copies; K and the row ring are local
+      const uint64_t t0 = global_timer_ns();
+      auto drain = [&](int base, int stages, int n) {
+        for (int u = max(0, n - stages); u < n; ++u)
+          while (!mbar_test_cl(bar(base + u % stages), (u / stages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      };
+      if (crank == 0) {
+        drain(C::kBarFullQ0, C::kQStages, nfq);
+        drain(C::kBarReQ0, C::kQStages, nrq);
+        drain(C::kBarFullD0, C::kDoStages, nfd);
+        drain(C::kBarReD0, C::kDoStages, nrd);
+        while (!mbar_test_cl(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+      while (!mbar_test(bar(C::kBarK), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
+        while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the rank-0 CTA's MMAs and both CTAs' copies are done with both CTAs' memory
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
 struct Dq256Cfg {
   static constexpr int D = 256;
   static constexpr int kTile = 128 * D * 2;
@@ -2714,9 +3190,22 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
       return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
     case 256: {
       const BwdParams q = with_kv_order(p, causal, 256);
-      const unsigned n = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.Hkv);  // (key tile, head-dim half)
+      // pairs: (key tile, CTA of the pair); else (key tile, head-dim half)
+      const unsigned n = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.Hkv);
       if (!n) return FA_ERR_UNSUPPORTED;
       const dim3 grid(n);
+      if (FA_DKDV256_PAIR) {
+        using PC = Dkdv256PairCfg;
+        if (causal)
+          return q.cu_seqlens ? launch_kernel(bwd_dkdv256_pair_kernel<true, true>, grid, PC::kThreads, PC::kSmemBytes,
+                                              q, stream)
+                              : launch_kernel(bwd_dkdv256_pair_kernel<true, false>, grid, PC::kThreads,
+                                              PC::kSmemBytes, q, stream);
+        return q.cu_seqlens ? launch_kernel(bwd_dkdv256_pair_kernel<false, true>, grid, PC::kThreads, PC::kSmemBytes,
+                                            q, stream)
+                            : launch_kernel(bwd_dkdv256_pair_kernel<false, false>, grid, PC::kThreads, PC::kSmemBytes,
+                                            q, stream);
+      }
       if (causal)
         return q.cu_seqlens ? launch_kernel(bwd_dkdv256_kernel<true, true>, grid, Dkdv256Cfg<true>::kThreads,
                                             Dkdv256Cfg<true>::kSmemBytes, q, stream)

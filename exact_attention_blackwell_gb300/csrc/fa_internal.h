@@ -50,9 +50,10 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
-  CUtensorMap tm_q64, tm_do64;          // the same tensors in boxes of 64 rows (CTA-pair dK/dV kernel)
-  CUtensorMap tm_k64, tm_v64;           // K, V in boxes of 64 rows (CTA-pair dQ kernel)
+  CUtensorMap tm_q64, tm_do64;          // the same tensors in boxes of 64 rows (CTA-pair kernels)
+  CUtensorMap tm_k64, tm_v64;           // K, V in boxes of 64 rows (CTA-pair kernels)
   CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
+  CUtensorMap tm_dk64, tm_dv64;         // the same in boxes of 64 rows (head-dim-256 CTA-pair dK/dV kernel)
   CUtensorMap tm_dq;                    // store [B, N, H, d]
   float *lse2;                          // [B, H, Npad] LSE * log2(e) (workspace)
   const float *delta;                   // [B, H, Npad] D = rowsum(dO * O) (workspace)

@@ -110,3 +110,56 @@ def test_cluster_scope_build_gives_the_same_bits(cluster_scope_lib, B, N, H, Hkv
     assert cluster_scope_lib.fa_last_device_status(None) == fa.FA_OK
     for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+
+
+# ---------------------------------------------------------------- head dim 256
+# The default library computes dK, dV at head dim 256 with CTA pairs of 64 keys
+# each (M = 128 pair MMAs, K in tensor memory, P^T and dS^T in shared memory);
+# a build with FA_DKDV256_PAIR=0 keeps one CTA per (key tile, head-dim half).
+@pytest.fixture(scope="module")
+def onecta256_lib(tmp_path_factory):
+    path = str(tmp_path_factory.mktemp("one256") / "libfa_one256.so")
+    build.build(force=True, extra_flags=["-DFA_DKDV256_PAIR=0"], lib_path=path)
+    lib = ctypes.CDLL(path)
+    for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_last_device_status"):
+        res, args = fa.SIGNATURES[name]
+        getattr(lib, name).restype = res
+        getattr(lib, name).argtypes = args
+    return lib
+
+
+CASES_256 = [
+    # B, N, H, Hkv, causal
+    (1, 64, 1, 1, False),    # the pair's second CTA holds no keys
+    (1, 200, 2, 1, True),    # ragged tail in the second CTA of the last pair, GQA
+    (2, 384, 2, 2, True),    # diagonal tiles: the second CTA's keys hide half the queries
+    (1, 1, 1, 1, True),      # a single row
+]
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,causal", CASES_256)
+def test_d256_pair_and_one_cta_match_oracle(oracle_mod, onecta256_lib, B, N, H, Hkv, causal):
+    d = 256
+    seed = 7900 + N + H + causal
+    q = inputs.random_bf16((B, N, H, d), seed, "cuda")
+    k = inputs.random_bf16((B, N, Hkv, d), seed + 1, "cuda")
+    v = inputs.random_bf16((B, N, Hkv, d), seed + 2, "cuda")
+    dO = inputs.random_bf16((B, N, H, d), seed + 3, "cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_fwd(q, k, v, scale=scale, causal=causal)
+    pair = fa.attention_bwd(q, k, v, o, lse, dO, scale=scale, causal=causal)
+    nb = onecta256_lib.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    one = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    st = onecta256_lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              dO.data_ptr(), one[0].data_ptr(), one[1].data_ptr(), one[2].data_ptr(), B, H, Hkv, N, d,
+                              scale, int(causal), ws.data_ptr(), nb, None)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert onecta256_lib.fa_last_device_status(None) == fa.FA_OK
+    assert fa.fa_last_device_status() == fa.FA_OK
+    ref = oracle_mod.attention_bwd(q.cpu(), k.cpu(), v.cpu(), dO.cpu(), scale, causal)
+    what = f"d256 B{B} N{N} H{H}/{Hkv} causal={causal}"
+    for name, a, b, r in zip(("dQ", "dK", "dV"), pair, one, ref):
+        check_grad(a.cpu(), r, f"pair {what} {name}")
+        check_grad(b.cpu(), r, f"one CTA {what} {name}")
