@@ -344,6 +344,7 @@ int setup_bwd(BwdParams *p, const void *q, const void *k, const void *v, const v
       (v && d >= 128 && encode_bf16_tile_map(&p->tm_v64, v, mb, mn, Hkv, d, 64)) ||
       (dk && d == 256 && encode_bf16_tile_map(&p->tm_dk64, dk, mb, mn, Hkv, d, 64)) ||
       (dv && d == 256 && encode_bf16_tile_map(&p->tm_dv64, dv, mb, mn, Hkv, d, 64)) ||
+      (dq && d == 256 && encode_bf16_tile_map(&p->tm_dq64, dq, mb, mn, H, d, 64)) ||
       (dq && encode_bf16_tile_map(&p->tm_dq, dq, mb, mn, H, d, 128)) ||
       (dk && encode_bf16_tile_map(&p->tm_dk, dk, mb, mn, Hkv, d, 128)) ||
       (dv && encode_bf16_tile_map(&p->tm_dv, dv, mb, mn, Hkv, d, 128)))

@@ -48,6 +48,11 @@
 #ifndef FA_DKDV256_PAIR
 #define FA_DKDV256_PAIR 1
 #endif
+// dQ at head dim 256 on CTA pairs of 64 query rows each (1, the default) or on
+// one CTA per query tile (0).
+#ifndef FA_DQ256_PAIR
+#define FA_DQ256_PAIR 1
+#endif
 
 namespace fa {
 namespace {
@@ -3066,6 +3071,369 @@ __global__ void __launch_bounds__(320, 1) bwd_dq256_kernel(const __grid_constant
   }
 }
 
+// ================================================================== dQ at head dim 256 on CTA pairs
+// Two CTAs of a cluster share one 128-row query tile, 64 query rows each, with
+// M = 128 `cta_group::2` MMAs issued by the rank-0 CTA (the TMEM and operand
+// layouts of the head-dim-256 dK/dV pair kernel above):
+//   S  = Q K_j^T    N = 128 keys: CTA c supplies key rows 64c..64c+63 (all d);
+//   dP = dO V_j^T   A = Q, dO from TMEM (copied once, both lane halves)
+//   dQ += dS K_j    N = 256 = d: CTA c supplies head-dim columns 128c..128c+127
+//                   of all keys; A = dS from shared memory (two buffers)
+// K_j streams as two quarter slots per stage, the one only S needed reloaded
+// in place for dQ; V_j only feeds dP.  TMEM: Q 128 | dO 128 | S 64 | dP 64 |
+// dQ 128 columns.  MMA order per key tile: S_j, dP_j, dQ_{j-1}; S and dP are
+// single-buffered, so the elementwise warps signal as soon as they have read them.
+struct Dq256PairCfg {
+  static constexpr int kBox = 64 * 128;        // 64 rows x 64 columns of bf16
+  static constexpr int kQuarter = 2 * kBox;    // 64 rows x 128 columns
+  static constexpr int kStage = 2 * kQuarter;  // two quarter slots
+  static constexpr int kKStages = 3, kVStages = 3, kDsBufs = 2;
+  static constexpr int kThreads = 320;
+  static constexpr int kMmaWarp = 8, kLoadWarp = 9;
+  static constexpr int kColQ = 0, kColDO = 128, kColS = 256, kColDP = 320, kColDQ = 384, kTmemCols = 512;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKStages * kStage;
+  static constexpr int kOffDS = kOffV + kVStages * kStage;     // dS buffers: 64 queries x 128 keys, 2 boxes each
+  static constexpr int kOffQTmp = kOffV + 2 * kStage;          // Q before its copy into TMEM: V stage 2
+  static constexpr int kOffDOTmp = kOffK + 2 * kStage;         // dO before its copy: K stage 2
+  enum { kBarQdo, kBarQT, kBarCopied, kBarFullK0, kBarEmptyK0 = kBarFullK0 + kKStages,
+         kBarReK0 = kBarEmptyK0 + kKStages, kBarSK0 = kBarReK0 + kKStages, kBarFullV0 = kBarSK0 + kKStages,
+         kBarEmptyV0 = kBarFullV0 + kVStages, kBarS = kBarEmptyV0 + kVStages, kBarDP, kBarSFree, kBarDPFree,
+         kBarDSFull0, kBarDSFree0 = kBarDSFull0 + kDsBufs, kBarFinal = kBarDSFree0 + kDsBufs, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffDS + kDsBufs * 2 * kBox;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Copies this thread's row m of a 64 x 256 bf16 tile (four 64-row boxes, 128-byte
+// swizzle) into TMEM as an A operand: boxes 2 wg, 2 wg + 1 to columns 32 bx.
+__device__ __forceinline__ void tile256_row_to_tmem(const uint8_t *tile, int m, int wg, uint32_t t_row) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int bx = 2 * wg + half;
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(tile + bx * 8192 + m * 128 + ((j ^ (m & 7)) * 16));
+      w[4 * j] = v.x;
+      w[4 * j + 1] = v.y;
+      w[4 * j + 2] = v.z;
+      w[4 * j + 3] = v.w;
+    }
+    tmem_st_32x32b_x32(t_row + 32 * bx, w);
+  }
+}
+
+template <bool CAUSAL, bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+    bwd_dq256_pair_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dq256PairCfg;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (!check_align(sbase, p.status)) return;  // same layout in both CTAs: both return
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int crank = (int)cluster_ctarank();
+  const int n_q = (p.N + 127) / 128;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_q, p.B * p.H, p.sched_chunk, rank, head);
+  const int it_q = CAUSAL ? n_q - 1 - rank : rank;  // causal: the longest tiles first
+  const int h = head % p.H, b = head / p.H;
+  const int kh = h / (p.H / p.Hkv);
+  const int Npad = n_q * 128;  // row-term arrays are [B, H, Npad]
+  const int q0 = it_q * 128;
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;
+  if (VARLEN && q0 >= L) return;  // the tile lies past its sequence (both CTAs return)
+  const int nb = CAUSAL ? it_q + 1 : (L + 127) / 128;
+  const int qrow0 = q0 + 64 * crank;  // this CTA's first query row
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i) {
+      const bool pair_warps = i == C::kBarQT || i == C::kBarSFree || i == C::kBarDPFree ||
+                              (i >= C::kBarDSFull0 && i < C::kBarDSFull0 + C::kDsBufs);
+      mbar_init(bar(i), pair_warps ? 16u : i == C::kBarCopied ? 8u : 1u);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q64);
+    prefetch_tmap(&p.tm_do64);
+    prefetch_tmap(&p.tm_k64);
+    prefetch_tmap(&p.tm_v64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const int m = r & 63, hk = r >> 6;  // query row of this CTA; key half of the S / dP columns
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int q_row = qrow0 + m;
+    const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
+    const float lse2 = p.lse2[rw];
+    const float dlt = p.delta[rw];
+    // ---- Q, dO -> TMEM (A of S, dP), row m in lanes m and 64 + m
+    bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
+    if (ok) {
+      tile256_row_to_tmem(smem + C::kOffQTmp, m, wg, tmem + lane_off + C::kColQ);
+      tile256_row_to_tmem(smem + C::kOffDOTmp, m, wg, tmem + lane_off + C::kColDO);
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();  // both regions are refilled by TMA after this
+    tc_fence_before();
+    mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarQT), 0));
+    mbar_arrive_warp(bar(C::kBarCopied));
+
+    const uint32_t s_tm = tmem + lane_off + C::kColS + 32 * wg;
+    const uint32_t dp_tm = tmem + lane_off + C::kColDP + 32 * wg;
+    const int kc0 = 64 * hk + 32 * wg;  // this thread's first key column within a key tile
+    const int last_key = CAUSAL ? min(q_row, L - 1) : L - 1;
+    for (int j = 0; j < nb && ok; ++j) {
+      ok = mbar_wait_warp_cl(bar(C::kBarS), j & 1, wctx, kBSiteS);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld_32x32b_x32(s_tm, sv);
+      tmem_wait_ld(sv);
+      tc_fence_before();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarSFree), 0));  // S is in registers: S_{j+1} may overwrite it
+      const int lim = last_key - (j * 128 + kc0);                   // last visible column offset
+      float pe[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), p.scale_log2, p.scale_log2, -lse2, -lse2);
+        pe[c] = ex2_mufu(x0);
+        pe[c + 1] = ex2_mufu(x1);
+      }
+      if (lim < 31) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c > lim) pe[c] = 0.f;
+      }
+      ok = mbar_wait_warp_cl(bar(C::kBarDP), j & 1, wctx, kBSiteDP);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dpv[32];
+      tmem_ld_32x32b_x32(dp_tm, dpv);
+      tmem_wait_ld(dpv);
+      tc_fence_before();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarDPFree), 0));
+      uint32_t wd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float t0, t1, d0, d1;
+        fadd2(t0, t1, __uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), -dlt, -dlt);
+        fmul2(d0, d1, pe[c], pe[c + 1], t0, t1);
+        wd[c >> 1] = pack_bf16x2(d0, d1);
+      }
+      const int db = j % C::kDsBufs;
+      if (j >= C::kDsBufs) {  // dQ_{j-2} has read this buffer
+        ok = mbar_wait_warp_cl(bar(C::kBarDSFree0 + db), ((j / C::kDsBufs) - 1) & 1, wctx, kBSiteDSFree);
+        if (!ok) break;
+      }
+      st_swizzled_32cols_r64(sbase + C::kOffDS + db * 2 * C::kBox, m, kc0, wd);
+      fence_proxy_async_smem();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarDSFull0 + db), 0));
+    }
+    // ---- epilogue: dQ * scale -> bf16 -> shared (the K ring) -> TMA store; warpgroup wg takes 64 of its 128 columns
+    if (ok) ok = mbar_wait_warp_cl(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
+    tc_fence_after();
+    const uint32_t acc_tm = tmem + lane_off + C::kColDQ;
+    const bool has_rows = qrow0 < L;
+    const bool direct = VARLEN && qrow0 + 64 > L;  // the next sequence's rows follow: write row by row
+    if (ok && has_rows && direct) {
+      acc_to_global<64>(acc_tm, static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)(sq.start + q_row) * p.H + h) * 256 +
+                                    128 * hk,
+                        64 * wg, p.scale, q_row < L);
+    } else if (ok && has_rows) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(acc_tm + 64 * wg + 32 * c, v);
+        tmem_wait_ld(v);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * p.scale, __uint_as_float(v[2 * k + 1]) * p.scale);
+        st_swizzled_32cols_r64(sbase + C::kOffK, m, 128 * hk + 64 * wg + 32 * c, w);
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 256);
+    if (threadIdx.x == 0 && ok && has_rows && !direct) {
+      for (int bx = 0; bx < 4; ++bx)
+        tma_store_4d(&p.tm_dq64, sbase + C::kOffK + bx * C::kBox, bx * 64, h, sq.start + qrow0, sq.bc);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    if (crank == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP (A in TMEM)
+      constexpr uint32_t id_o = make_idesc_bf16(128, 256, false, true);   // dQ (B MN-major)
+      const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffK, 0, 1024);
+      const uint64_t k_mn = make_sdesc_sw128(sbase + C::kOffK, C::kBox, 1024);
+      const uint64_t v_d = make_sdesc_sw128(sbase + C::kOffV, 0, 1024);
+      const uint64_t ds_d = make_sdesc_sw128(sbase + C::kOffDS, 0, 1024);
+      auto kmaj = [](int kk) { return (uint64_t)(((kk >> 2) * C::kBox + (kk & 3) * 32) >> 4); };
+      auto off = [](int bytes) { return (uint64_t)(bytes >> 4); };
+      bool ok = mbar_wait_warp_cl(bar(C::kBarQT), 0, wctx, kBSiteQ);
+      for (int jj = 0; jj <= nb && ok; ++jj) {
+        if (jj < nb) {
+          const int sk = jj % C::kKStages, sv = jj % C::kVStages;
+          ok = mbar_wait_warp_cl(bar(C::kBarFullK0 + sk), (jj / C::kKStages) & 1, wctx, kBSiteFull);
+          if (ok && jj > 0) ok = mbar_wait_warp_cl(bar(C::kBarSFree), (jj - 1) & 1, wctx, kBSiteSL);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {  // S = Q K^T: head-dim half kk / 8 of this CTA's key rows
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_ts_pair(tmem + C::kColS, tmem + C::kColQ + 8 * kk,
+                          k_d + off(sk * C::kStage + (kk >> 3) * C::kQuarter) + kmaj(kk & 7), id_s, kk > 0);
+            tc_commit_pair(bar(C::kBarS));
+            tc_commit_pair(bar(C::kBarSK0 + sk));
+          }
+          __syncwarp();
+          ok = mbar_wait_warp_cl(bar(C::kBarFullV0 + sv), (jj / C::kVStages) & 1, wctx, kBSiteFull);
+          if (ok && jj > 0) ok = mbar_wait_warp_cl(bar(C::kBarDPFree), (jj - 1) & 1, wctx, kBSiteSL);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {  // dP = dO V^T
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_ts_pair(tmem + C::kColDP, tmem + C::kColDO + 8 * kk,
+                          v_d + off(sv * C::kStage + (kk >> 3) * C::kQuarter) + kmaj(kk & 7), id_s, kk > 0);
+            tc_commit_pair(bar(C::kBarDP));
+            tc_commit_pair(bar(C::kBarEmptyV0 + sv));
+          }
+          __syncwarp();
+        }
+        if (jj > 0) {  // dQ += dS K of the previous key tile (its second K quarter reloaded)
+          const int j = jj - 1, sk = j % C::kKStages, db = j % C::kDsBufs;
+          ok = mbar_wait_warp_cl(bar(C::kBarDSFull0 + db), (j / C::kDsBufs) & 1, wctx, kBSiteDS);
+          if (ok) ok = mbar_wait_warp_cl(bar(C::kBarReK0 + sk), (j / C::kKStages) & 1, wctx, kBSiteFull);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss_pair(tmem + C::kColDQ, ds_d + off(db * 2 * C::kBox) + kmaj(kk),
+                          k_mn + off(sk * C::kStage + (kk >> 2) * C::kQuarter + (kk & 3) * 2048), id_o,
+                          (j > 0 || kk > 0));
+            tc_commit_pair(bar(C::kBarDSFree0 + db));
+            tc_commit_pair(bar(C::kBarEmptyK0 + sk));
+          }
+          __syncwarp();
+        }
+      }
+      if (elect_one()) {
+        tc_commit_pair(bar(C::kBarFinal));
+        tc_commit_pair(bar(C::kBarDrain));
+      }
+      __syncwarp();
+      if (!mbar_wait_warp_cl(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test_cl(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer (both CTAs; stage bytes counted by rank 0)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint64_t once = policy_evict_first();
+      mbar_arrive_expect_tx(bar(C::kBarQdo), 8 * C::kBox);
+      for (int bx = 0; bx < 4; ++bx) {
+        tma_load_4d_hint(sbase + C::kOffQTmp + bx * C::kBox, &p.tm_q64, bar(C::kBarQdo), bx * 64, h, sq.start + qrow0,
+                         sq.bc, once);
+        tma_load_4d_hint(sbase + C::kOffDOTmp + bx * C::kBox, &p.tm_do64, bar(C::kBarQdo), bx * 64, h,
+                         sq.start + qrow0, sq.bc, once);
+      }
+      bool ok = true;
+      int nfk = 0, nrk = 0, nfv = 0;
+      for (int j = 0; j <= nb && ok; ++j) {
+        const int kv_row = sq.start + j * 128;
+        if (j < nb) {  // K_j: this CTA's key half, both head-dim halves
+          const int sk = j % C::kKStages;
+          if (j == 2) {  // K stage 2 and V stage 2 held dO and Q
+            ok = mbar_wait(bar(C::kBarCopied), 0, wctx, kBSiteQ);
+            if (!ok) break;
+          }
+          ok = mbar_wait_cl(bar(C::kBarEmptyK0 + sk), ((j / C::kKStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFullK0 + sk), 2 * C::kStage);
+          const uint32_t fb = mapa_shared(bar(C::kBarFullK0 + sk), 0);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_4d_pair(sbase + C::kOffK + sk * C::kStage + dh * C::kQuarter + bx * C::kBox, &p.tm_k64, fb,
+                               128 * dh + 64 * bx, kh, kv_row + 64 * crank, sq.bc, keep);
+          ++nfk;
+        }
+        if (j > 0) {  // reload for the previous tile: the other key half, this CTA's head-dim half
+          const int jp = j - 1, sk = jp % C::kKStages;
+          ok = mbar_wait_cl(bar(C::kBarSK0 + sk), (jp / C::kKStages) & 1, wctx, kBSiteS);  // S_jp has read the slot
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarReK0 + sk), 2 * C::kQuarter);
+          const uint32_t rk = mapa_shared(bar(C::kBarReK0 + sk), 0);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(sbase + C::kOffK + sk * C::kStage + (1 - crank) * C::kQuarter + bx * C::kBox, &p.tm_k64,
+                             rk, 128 * crank + 64 * bx, kh, sq.start + jp * 128 + 64 * (1 - crank), sq.bc, keep);
+          ++nrk;
+        }
+        if (j < nb) {  // V_j: this CTA's key half, both head-dim halves
+          const int sv = j % C::kVStages;
+          ok = mbar_wait_cl(bar(C::kBarEmptyV0 + sv), ((j / C::kVStages) & 1) ^ 1, wctx, kBSiteEmpty);
+          if (!ok) break;
+          if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFullV0 + sv), 2 * C::kStage);
+          const uint32_t fb = mapa_shared(bar(C::kBarFullV0 + sv), 0);
+          for (int dh = 0; dh < 2; ++dh)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_4d_pair(sbase + C::kOffV + sv * C::kStage + dh * C::kQuarter + bx * C::kBox, &p.tm_v64, fb,
+                               128 * dh + 64 * bx, kh, kv_row + 64 * crank, sq.bc, keep);
+          ++nfv;
+        }
+      }
+      // drain: the stage barriers of rank 0 count both CTAs' copies; Q / dO are local
+      const uint64_t t0 = global_timer_ns();
+      auto drain = [&](int base, int stages, int n) {
+        for (int u = max(0, n - stages); u < n; ++u)
+          while (!mbar_test_cl(bar(base + u % stages), (u / stages) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      };
+      if (crank == 0) {
+        drain(C::kBarFullK0, C::kKStages, nfk);
+        drain(C::kBarReK0, C::kKStages, nrk);
+        drain(C::kBarFullV0, C::kVStages, nfv);
+      }
+      while (!mbar_test(bar(C::kBarQdo), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the rank-0 CTA's MMAs and both CTAs' copies are done with both CTAs' memory
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ launches
 template <typename Kern>
 int launch_kernel(Kern kern, dim3 grid, int threads, int smem, const BwdParams &p, cudaStream_t stream) {
@@ -3247,6 +3615,20 @@ int launch_bwd_dq(const BwdParams &p, int d, bool causal, cudaStream_t stream) {
       const BwdParams q = with_q_order(p, causal, 256);
       const unsigned n = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
       if (!n) return FA_ERR_UNSUPPORTED;
+      if (FA_DQ256_PAIR) {
+        using PC = Dq256PairCfg;
+        const unsigned n2 = grid_1d(2 * ((p.N + 127) / 128), (long long)p.B * p.H);  // (query tile, CTA of the pair)
+        if (!n2) return FA_ERR_UNSUPPORTED;
+        if (causal)
+          return q.cu_seqlens ? launch_kernel(bwd_dq256_pair_kernel<true, true>, dim3(n2), PC::kThreads,
+                                              PC::kSmemBytes, q, stream)
+                              : launch_kernel(bwd_dq256_pair_kernel<true, false>, dim3(n2), PC::kThreads,
+                                              PC::kSmemBytes, q, stream);
+        return q.cu_seqlens ? launch_kernel(bwd_dq256_pair_kernel<false, true>, dim3(n2), PC::kThreads, PC::kSmemBytes,
+                                            q, stream)
+                            : launch_kernel(bwd_dq256_pair_kernel<false, false>, dim3(n2), PC::kThreads,
+                                            PC::kSmemBytes, q, stream);
+      }
       const dim3 grid(n);
       if (causal)
         return q.cu_seqlens ? launch_kernel(bwd_dq256_kernel<true, true>, grid, Dq256Cfg::kThreads, Dq256Cfg::kSmemBytes,

@@ -55,6 +55,7 @@ struct BwdParams {
   CUtensorMap tm_dk, tm_dv;             // stores [B, N, Hkv, d]
   CUtensorMap tm_dk64, tm_dv64;         // the same in boxes of 64 rows (head-dim-256 CTA-pair dK/dV kernel)
   CUtensorMap tm_dq;                    // store [B, N, H, d]
+  CUtensorMap tm_dq64;                  // the same in boxes of 64 rows (head-dim-256 CTA-pair dQ kernel)
   float *lse2;                          // [B, H, Npad] LSE * log2(e) (workspace)
   const float *delta;                   // [B, H, Npad] D = rowsum(dO * O) (workspace)
   unsigned *status;

@@ -113,13 +113,15 @@ def test_cluster_scope_build_gives_the_same_bits(cluster_scope_lib, B, N, H, Hkv
 
 
 # ---------------------------------------------------------------- head dim 256
-# The default library computes dK, dV at head dim 256 with CTA pairs of 64 keys
-# each (M = 128 pair MMAs, K in tensor memory, P^T and dS^T in shared memory);
-# a build with FA_DKDV256_PAIR=0 keeps one CTA per (key tile, head-dim half).
+# The default library computes the head-dim-256 backward with CTA pairs: dK, dV
+# with 64 keys per CTA (M = 128 pair MMAs, K in tensor memory, P^T and dS^T in
+# shared memory) and dQ with 64 query rows per CTA (Q, dO in tensor memory).  A
+# build with FA_DKDV256_PAIR=0 and FA_DQ256_PAIR=0 keeps one CTA per (key tile,
+# head-dim half) and one CTA per query tile.
 @pytest.fixture(scope="module")
 def onecta256_lib(tmp_path_factory):
     path = str(tmp_path_factory.mktemp("one256") / "libfa_one256.so")
-    build.build(force=True, extra_flags=["-DFA_DKDV256_PAIR=0"], lib_path=path)
+    build.build(force=True, extra_flags=["-DFA_DKDV256_PAIR=0", "-DFA_DQ256_PAIR=0"], lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_last_device_status"):
         res, args = fa.SIGNATURES[name]
