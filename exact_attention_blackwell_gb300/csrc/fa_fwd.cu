@@ -488,6 +488,360 @@ __global__ void __launch_bounds__(FwdCfg<D, QT_>::kThreads, FwdCfg<D, QT_>::kMin
   if (threadIdx.x == 0) FA_LIFE(6);
 }
 
+// ================================================================== head dim 256 on CTA pairs
+// At head dim 256 one query tile per CTA is all TMEM holds (S 128 + O 256
+// columns), so the kernel above serialises S_j -> softmax_j -> PV_j, and each
+// key block brings 128 KB of K and V into one SM.  Here two CTAs of a cluster
+// share 256 query rows (128 each) and the rank-0 CTA issues M = 256
+// `cta_group::2` MMAs (FA4 paper summary, section 2.C: each SM holds its own
+// rows of A and half of B):
+//   S_j  = Q K_j^T   N = 128 keys: CTA c loads key rows 64c..64c+63 (32 KB)
+//   O   += P_j V_j   N = 256 = d: CTA c loads head-dim columns 128c..128c+127
+//                    of all 128 keys (32 KB); P_j read from TMEM
+// TMEM per CTA: S in two buffers (columns 0 and 128) and O (256 columns), so
+// S_{j+1} runs on the tensor core while the softmax works on S_j.  MMA order:
+// S_0 S_1 | PV_0 S_2 | PV_1 S_3 | ...  With S_{j+1} already issued when the
+// softmax meets block j, a rescale of O first waits for PV_{j-1}.
+struct Fwd256PairCfg {
+  static constexpr int D = 256;
+  static constexpr int kTileBytes = 128 * D * 2;  // the CTA's Q tile: four 128-row boxes
+  static constexpr int kHalf = 32768;  // K half: 64 rows x 256 (4 boxes); V half: 128 rows x 128 (2 boxes)
+  static constexpr int kStages = 5;
+  static constexpr int kThreads = 192;  // 4 softmax warps, MMA warp, TMA warp
+  static constexpr int kMmaWarp = 4, kLoadWarp = 5;
+  static constexpr int kColO = 256, kTmemCols = 512;  // S_j in columns 128 (j % 2)
+  static constexpr int kOffQ = 0, kOffRing = kTileBytes;
+  enum { kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarQ = kBarEmpty0 + kStages, kBarS0, kBarP0 = kBarS0 + 2,
+         kBarPV = kBarP0 + 2, kBarO, kBarDrain, kNumBars };
+  static constexpr int kOffBar = kOffRing + kStages * kHalf;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+template <bool CAUSAL, bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    fa_fwd256_pair_kernel(const __grid_constant__ FwdParams p) {
+  using C = Fwd256PairCfg;
+  constexpr int D = 256;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // same layout in both CTAs: both return before any cluster work
+    if (threadIdx.x == 0) {
+      atomicOr(p.status, 1u);
+      atomicCAS(p.status + 1, 0u, (unsigned)kSiteQ);
+    }
+    return;
+  }
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  const WaitCtx wctx{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int crank = (int)cluster_ctarank();
+  const int n_q = (p.N + 127) / 128;
+  const int n_pairs = (n_q + 1) / 2;
+  int rank, head;
+  work_order((int)(blockIdx.x >> 1), n_pairs, p.B * p.H, p.sched_chunk, rank, head);
+  const int pg = CAUSAL ? n_pairs - 1 - rank : rank;  // causal: the longest query rows first
+  const int h = head % p.H, b = head / p.H;
+  const int kh = h / (p.H / p.Hkv);
+  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
+  const int L = sq.len;
+  const int qp0 = 256 * pg;  // the pair's first query row
+  if (VARLEN && qp0 >= L) return;  // both CTAs return
+  const int q0 = qp0 + 128 * crank;  // this CTA's query tile
+  // key blocks: the pair computes every block its later tile needs; the earlier
+  // tile's rows mask the last one whole under the causal mask
+  const int nb = CAUSAL ? min(qp0 + 255, L - 1) / 128 + 1 : (L + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumBars; ++i)  // P collects one arrival per softmax warp of both CTAs
+      mbar_init(bar(i), (i == C::kBarP0 || i == C::kBarP0 + 1) ? 8u : 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::kLoadWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k64);
+    prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ===================================================== softmax (one thread per query row of this CTA)
+    const int r = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t o_tm = tmem + lane_off + C::kColO;
+    const int q_row = q0 + r;
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    unsigned rescales = 0;
+    for (int j = 0; j < nb && ok; ++j) {
+      const int sb = j & 1;
+      const uint32_t s_tm = tmem + lane_off + 128u * sb;
+      ok = mbar_wait_warp_cl(bar(C::kBarS0 + sb), (j >> 1) & 1, wctx, kSiteSFull);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(s_tm + 32 * c, sr[c]);
+      tmem_wait_ld(sr[0]);
+      reg_tie(sr[1]);
+      reg_tie(sr[2]);
+      reg_tie(sr[3]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      const int kv0 = j * 128;
+      const int lim = (CAUSAL ? min(L - 1, q_row) : L - 1) - kv0;  // last visible column
+      if (__any_sync(0xffffffffu, lim < 127)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 124; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+      }
+      mx0 = fmax3(mx0, s[124], s[125]);
+      mx1 = fmax3(mx1, s[126], s[127]);
+      const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c2;
+      if (j == 0) {
+        m_ref = m_blk;
+      } else {
+        const bool need = (m_blk - m_ref) > kRescaleTau;
+        if (__any_sync(0xffffffffu, need)) {
+          // PV_{j-1} must have landed in O before it is scaled (S_j was issued before it)
+          ok = mbar_wait_warp_cl(bar(C::kBarPV), (j - 1) & 1, wctx, kSiteOFull);
+          if (!ok) break;
+          tc_fence_after();
+          const float m_new = fmaxf(m_ref, m_blk);
+          const float alpha = ex2_mufu(m_ref - m_new);
+          m_ref = m_new;
+          l_sum *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(o_tm + 16 * c, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_32x32b_x16(o_tm + 16 * c, o);
+          }
+          rescales += (lane == 0);
+        }
+      }
+      const float neg_m = -m_ref;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          float x[4], e[4];
+          ffma2(x[0], x[1], s[64 * half + c], s[64 * half + c + 1], c2, c2, neg_m, neg_m);
+          ffma2(x[2], x[3], s[64 * half + c + 2], s[64 * half + c + 3], c2, c2, neg_m, neg_m);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) e[u] = ((c + u) % 16 < FA_FWD_POLY_PER16) ? exp2_poly(x[u]) : ex2_mufu(x[u]);
+          fadd2(l0, l1, l0, l1, e[0], e[1]);
+          fadd2(l2, l3, l2, l3, e[2], e[3]);
+          pk[c >> 1] = pack_bf16x2(e[0], e[1]);
+          pk[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
+        }
+        tmem_st_32x32b_x32(s_tm + 32 * half, pk);
+      }
+      l_sum += (l0 + l1) + (l2 + l3);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp_cluster(mapa_shared(bar(C::kBarP0 + sb), 0));
+    }
+    // ----------------------------------------------------- epilogue (this CTA's 128 rows)
+    if (ok) ok = mbar_wait_warp_cl(bar(C::kBarO), 0, wctx, kSiteOFull);
+    tc_fence_after();
+    uint8_t *stage = smem + C::kOffQ;  // Q is dead once O is final
+    const bool has_rows = q0 < L;
+    const bool direct = VARLEN && q0 + 128 > L;
+    if (ok && has_rows) {
+      const float inv_l = 1.0f / l_sum;
+      uint4 *orow = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + ((size_t)(sq.start + q_row) * p.H + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(o_tm + 32 * c, o);
+        tmem_wait_ld(o);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (direct) {
+          if (q_row < L) {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) orow[4 * c + k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int chunk = ((c & 1) * 4 + k4) ^ (r & 7);
+            *reinterpret_cast<uint4 *>(stage + (c >> 1) * 16384 + r * 128 + chunk * 16) =
+                make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+          }
+        }
+      }
+      if (p.lse != nullptr && q_row < L) {
+        const size_t li = VARLEN ? (size_t)h * p.total + sq.start + q_row : ((size_t)b * p.H + h) * p.N + q_row;
+        p.lse[li] = (m_ref + __log2f(l_sum)) * 0.69314718055994531f;
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (r == 0 && ok && has_rows && !direct) {
+      for (int bx = 0; bx < 4; ++bx) tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+    if (rescales) atomicAdd(p.status + 2, rescales);
+  } else if (warp == C::kMmaWarp) {
+    // ===================================================== MMA issue (rank-0 CTA, for both)
+    if (crank == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(256, 128, false, false);
+      constexpr uint32_t id_pv = make_idesc_bf16(256, D, false, true);
+      const uint64_t q_d = make_sdesc_sw128(sbase + C::kOffQ, 0, 1024);
+      const uint64_t k_d = make_sdesc_sw128(sbase + C::kOffRing, 0, 1024);
+      const uint64_t v_mn = make_sdesc_sw128(sbase + C::kOffRing, 16384, 1024);
+      auto slot_of = [](int fill) { return fill % C::kStages; };
+      auto full_ok = [&](int fill) {
+        return mbar_wait_warp_cl(bar(C::kBarFull0 + slot_of(fill)), (uint32_t)((fill / C::kStages) & 1), wctx,
+                                 (fill & 1) ? kSiteVFull : kSiteKFull);
+      };
+      auto issue_s = [&](int j) {  // S_j into buffer j % 2; K_j is fill 2 j
+        const uint64_t kd = k_d + (uint64_t)((slot_of(2 * j) * C::kHalf) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss_pair(tmem + 128u * (j & 1), q_d + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                        kd + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id_s, kk > 0);
+          tc_commit_pair(bar(C::kBarS0 + (j & 1)));
+          tc_commit_pair(bar(C::kBarEmpty0 + slot_of(2 * j)));
+        }
+        __syncwarp();
+      };
+      bool ok = mbar_wait_warp_cl(bar(C::kBarQ), 0, wctx, kSiteQ);
+      for (int j = 0; j < 2 && j < nb && ok; ++j) {
+        ok = full_ok(2 * j);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(j);
+      }
+      for (int j = 0; j < nb && ok; ++j) {
+        ok = full_ok(2 * j + 1);
+        if (ok) ok = mbar_wait_warp_cl(bar(C::kBarP0 + (j & 1)), (j >> 1) & 1, wctx, kSitePFull);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {  // O += P_j V_j
+          const uint64_t vd = v_mn + (uint64_t)((slot_of(2 * j + 1) * C::kHalf) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_pair(tmem + C::kColO, tmem + 128u * (j & 1) + 8u * kk, vd + (uint64_t)(kk * 128), id_pv,
+                        (j > 0 || kk > 0));
+          tc_commit_pair(bar(C::kBarPV));
+          tc_commit_pair(bar(C::kBarEmpty0 + slot_of(2 * j + 1)));
+          if (j + 1 == nb) tc_commit_pair(bar(C::kBarO));
+        }
+        __syncwarp();
+        if (j + 2 < nb) {  // S_{j+2} over P_j (its PV was issued first)
+          ok = full_ok(2 * j + 4);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(j + 2);
+        }
+      }
+      if (elect_one()) tc_commit_pair(bar(C::kBarDrain));
+      __syncwarp();
+      if (!mbar_wait_warp_cl(bar(C::kBarDrain), 0, wctx, kSiteDrain) && *abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test_cl(bar(C::kBarDrain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else {
+    // ===================================================== TMA producer (both CTAs; bytes counted by rank 0)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      const uint64_t once = policy_evict_first();
+      if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
+      const uint32_t qb = mapa_shared(bar(C::kBarQ), 0);
+      for (int bx = 0; bx < 4; ++bx)
+        tma_load_4d_pair(sbase + C::kOffQ + bx * 16384, &p.tm_q, qb, bx * 64, h, sq.start + q0, sq.bc, once);
+      bool ok = true;
+      int fill = 0;
+      for (; fill < 2 * nb && ok; ++fill) {
+        const int j = fill >> 1, s = fill % C::kStages;
+        ok = mbar_wait_cl(bar(C::kBarEmpty0 + s), ((fill / C::kStages) & 1) ^ 1, wctx, kSiteEmpty);
+        if (!ok) break;
+        if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFull0 + s), 2 * C::kHalf);
+        const uint32_t fb = mapa_shared(bar(C::kBarFull0 + s), 0);
+        const uint32_t dst = sbase + C::kOffRing + s * C::kHalf;
+        if ((fill & 1) == 0) {  // K_j: this CTA's 64 key rows, all 256 columns
+          for (int bx = 0; bx < 4; ++bx)
+            tma_load_4d_pair(dst + bx * 8192, &p.tm_k64, fb, bx * 64, kh, sq.start + 128 * j + 64 * crank, sq.bc, keep);
+        } else {  // V_j: all 128 key rows, this CTA's head-dim half
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_4d_pair(dst + bx * 16384, &p.tm_v, fb, 128 * crank + 64 * bx, kh, sq.start + 128 * j, sq.bc, keep);
+        }
+      }
+      // drain: rank 0's barriers count both CTAs' copies
+      if (crank == 0) {
+        const uint64_t t0 = global_timer_ns();
+        for (int f = max(0, fill - C::kStages); f < fill; ++f)
+          while (!mbar_test_cl(bar(C::kBarFull0 + f % C::kStages), (f / C::kStages) & 1) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {}
+        while (!mbar_test_cl(bar(C::kBarQ), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the rank-0 CTA's MMAs and both CTAs' copies are done with both CTAs' memory
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
+template <bool CAUSAL, bool VARLEN>
+int launch_fwd256_pair(const FwdParams &p_in, cudaStream_t stream) {
+  using C = Fwd256PairCfg;
+  auto kern = fa_fwd256_pair_kernel<CAUSAL, VARLEN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const long long n_pairs = ((p_in.N + 127) / 128 + 1) / 2;
+  const long long n_ctas = 2 * n_pairs * p_in.H * p_in.B;
+  if (n_ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  FwdParams p = p_in;
+  const int g = p.H / p.Hkv;
+  p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * 256 * 2, p.B * p.Hkv) : 1;
+  kern<<<(unsigned)n_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <int D, bool CAUSAL, bool VARLEN, int QT>
 int launch_fwd_q(const FwdParams &p_in, cudaStream_t stream) {
   using C = FwdCfg<D, QT>;
@@ -517,10 +871,18 @@ int launch_fwd_q(const FwdParams &p_in, cudaStream_t stream) {
 #define FA_FWD_SHORT_MAX_N_D64 4096
 #endif
 
+// Head dim 256 on CTA pairs (1, the default) or one query tile per CTA (0).
+#ifndef FA_FWD256_PAIR
+#define FA_FWD256_PAIR 1
+#endif
+
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_fwd_v(const FwdParams &p, cudaStream_t stream) {
   if constexpr (D == 64) {
     if (p.N <= FA_FWD_SHORT_MAX_N_D64) return launch_fwd_q<D, CAUSAL, VARLEN, 1>(p, stream);
+  }
+  if constexpr (D == 256) {
+    if (FA_FWD256_PAIR) return launch_fwd256_pair<CAUSAL, VARLEN>(p, stream);
   }
   return launch_fwd_q<D, CAUSAL, VARLEN, FwdCfg<D>::kQT>(p, stream);
 }
