@@ -178,7 +178,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   std::memset(&p, 0, sizeof(p));
   if (encode_bf16_tile_map(&p.tm_q, q, B, N, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, B, N, Hkv, d, 128) ||
       encode_bf16_tile_map(&p.tm_v, v, B, N, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_o, o, B, N, H, d, 128) ||
-      (d == 256 && encode_bf16_tile_map(&p.tm_k64, k, B, N, Hkv, d, 64)))
+      (d >= 128 && encode_bf16_tile_map(&p.tm_k64, k, B, N, Hkv, d, 64)))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;
@@ -208,7 +208,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
   // the packed tensors as one batch of `total` rows
   if (encode_bf16_tile_map(&p.tm_q, q, 1, total, H, d, 128) || encode_bf16_tile_map(&p.tm_k, k, 1, total, Hkv, d, 128) ||
       encode_bf16_tile_map(&p.tm_v, v, 1, total, Hkv, d, 128) || encode_bf16_tile_map(&p.tm_o, o, 1, total, H, d, 128) ||
-      (d == 256 && encode_bf16_tile_map(&p.tm_k64, k, 1, total, Hkv, d, 64)))
+      (d >= 128 && encode_bf16_tile_map(&p.tm_k64, k, 1, total, Hkv, d, 64)))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;

@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(FwdCfg<D, QT_>::kThreads, FwdCfg<D, QT_>::kMin
   if (threadIdx.x == 0) FA_LIFE(6);
 }
 
-// ================================================================== head dim 256 on CTA pairs
+// ================================================================== CTA pairs (head dim 256)
 // At head dim 256 one query tile per CTA is all TMEM holds (S 128 + O 256
 // columns), so the kernel above serialises S_j -> softmax_j -> PV_j, and each
 // key block brings 128 KB of K and V into one SM.  Here two CTAs of a cluster
@@ -502,11 +502,12 @@ __global__ void __launch_bounds__(FwdCfg<D, QT_>::kThreads, FwdCfg<D, QT_>::kMin
 // S_{j+1} runs on the tensor core while the softmax works on S_j.  MMA order:
 // S_0 S_1 | PV_0 S_2 | PV_1 S_3 | ...  With S_{j+1} already issued when the
 // softmax meets block j, a rescale of O first waits for PV_{j-1}.
-struct Fwd256PairCfg {
-  static constexpr int D = 256;
-  static constexpr int kTileBytes = 128 * D * 2;  // the CTA's Q tile: four 128-row boxes
-  static constexpr int kHalf = 32768;  // K half: 64 rows x 256 (4 boxes); V half: 128 rows x 128 (2 boxes)
-  static constexpr int kStages = 5;
+template <int D>
+struct FwdPairCfg {
+  static constexpr int kTileBytes = 128 * D * 2;  // the CTA's Q tile: D / 64 boxes of 128 rows
+  // K half: 64 rows x D (D / 64 boxes of 8 KB); V half: 128 rows x D / 2 (D / 128 boxes of 16 KB)
+  static constexpr int kHalf = 64 * D * 2;
+  static constexpr int kStages = (232448 - kTileBytes - 256) / kHalf;  // 5 at D = 256, 12 at D = 128
   static constexpr int kThreads = 192;  // 4 softmax warps, MMA warp, TMA warp
   static constexpr int kMmaWarp = 4, kLoadWarp = 5;
   static constexpr int kColO = 256, kTmemCols = 512;  // S_j in columns 128 (j % 2)
@@ -519,11 +520,10 @@ struct Fwd256PairCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    fa_fwd256_pair_kernel(const __grid_constant__ FwdParams p) {
-  using C = Fwd256PairCfg;
-  constexpr int D = 256;
+    fa_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdPairCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // same layout in both CTAs: both return before any cluster work
@@ -694,7 +694,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (direct) {
           if (q_row < L) {
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) orow[4 * c + k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
+            for (int k4 = 0; k4 < 4; ++k4)
+              orow[4 * c + k4] = make_uint4(w[4 * k4], w[4 * k4 + 1], w[4 * k4 + 2], w[4 * k4 + 3]);
           }
         } else {
 #pragma unroll
@@ -713,7 +714,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
     if (r == 0 && ok && has_rows && !direct) {
-      for (int bx = 0; bx < 4; ++bx) tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_store_4d(&p.tm_o, smem_u32(stage) + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -787,7 +789,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       const uint64_t once = policy_evict_first();
       if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kTileBytes);
       const uint32_t qb = mapa_shared(bar(C::kBarQ), 0);
-      for (int bx = 0; bx < 4; ++bx)
+      for (int bx = 0; bx < D / 64; ++bx)
         tma_load_4d_pair(sbase + C::kOffQ + bx * 16384, &p.tm_q, qb, bx * 64, h, sq.start + q0, sq.bc, once);
       bool ok = true;
       int fill = 0;
@@ -798,12 +800,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (crank == 0) mbar_arrive_expect_tx(bar(C::kBarFull0 + s), 2 * C::kHalf);
         const uint32_t fb = mapa_shared(bar(C::kBarFull0 + s), 0);
         const uint32_t dst = sbase + C::kOffRing + s * C::kHalf;
-        if ((fill & 1) == 0) {  // K_j: this CTA's 64 key rows, all 256 columns
-          for (int bx = 0; bx < 4; ++bx)
+        if ((fill & 1) == 0) {  // K_j: this CTA's 64 key rows, all D columns
+          for (int bx = 0; bx < D / 64; ++bx)
             tma_load_4d_pair(dst + bx * 8192, &p.tm_k64, fb, bx * 64, kh, sq.start + 128 * j + 64 * crank, sq.bc, keep);
         } else {  // V_j: all 128 key rows, this CTA's head-dim half
-          for (int bx = 0; bx < 2; ++bx)
-            tma_load_4d_pair(dst + bx * 16384, &p.tm_v, fb, 128 * crank + 64 * bx, kh, sq.start + 128 * j, sq.bc, keep);
+          for (int bx = 0; bx < D / 128; ++bx)
+            tma_load_4d_pair(dst + bx * 16384, &p.tm_v, fb, (D / 2) * crank + 64 * bx, kh, sq.start + 128 * j, sq.bc,
+                             keep);
         }
       }
       // drain: rank 0's barriers count both CTAs' copies
@@ -826,10 +829,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   }
 }
 
-template <bool CAUSAL, bool VARLEN>
-int launch_fwd256_pair(const FwdParams &p_in, cudaStream_t stream) {
-  using C = Fwd256PairCfg;
-  auto kern = fa_fwd256_pair_kernel<CAUSAL, VARLEN>;
+template <int D, bool CAUSAL, bool VARLEN>
+int launch_fwd_pair(const FwdParams &p_in, cudaStream_t stream) {
+  using C = FwdPairCfg<D>;
+  auto kern = fa_fwd_pair_kernel<D, CAUSAL, VARLEN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
   const long long n_pairs = ((p_in.N + 127) / 128 + 1) / 2;
@@ -837,7 +840,7 @@ int launch_fwd256_pair(const FwdParams &p_in, cudaStream_t stream) {
   if (n_ctas > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   FwdParams p = p_in;
   const int g = p.H / p.Hkv;
-  p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * 256 * 2, p.B * p.Hkv) : 1;
+  p.sched_chunk = CAUSAL ? g * sched_chunk_for(true, (size_t)2 * p.N * D * 2, p.B * p.Hkv) : 1;
   kern<<<(unsigned)n_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -875,15 +878,23 @@ int launch_fwd_q(const FwdParams &p_in, cudaStream_t stream) {
 #ifndef FA_FWD256_PAIR
 #define FA_FWD256_PAIR 1
 #endif
+// Head dim 128 on CTA pairs (1) or two query tiles per CTA (0, the default).
+// The pair form passes the forward tests but measured 5-45 % slower on GB300
+// (headline 1.34 against 1.28 ms, causal B8 N4096 0.48 against 0.40 ms,
+// N = 1024 0.32 against 0.24 ms): at this head dim one softmax warpgroup per
+// 128 rows cannot keep up with MMAs half as long as at 256, and the two-tile
+// CTA overlaps one tile's softmax with the other's MMAs.
+#ifndef FA_FWD128_PAIR
+#define FA_FWD128_PAIR 0
+#endif
 
 template <int D, bool CAUSAL, bool VARLEN>
 int launch_fwd_v(const FwdParams &p, cudaStream_t stream) {
   if constexpr (D == 64) {
     if (p.N <= FA_FWD_SHORT_MAX_N_D64) return launch_fwd_q<D, CAUSAL, VARLEN, 1>(p, stream);
   }
-  if constexpr (D == 256) {
-    if (FA_FWD256_PAIR) return launch_fwd256_pair<CAUSAL, VARLEN>(p, stream);
-  }
+  if constexpr (D == 256 && FA_FWD256_PAIR) return launch_fwd_pair<256, CAUSAL, VARLEN>(p, stream);
+  if constexpr (D == 128 && FA_FWD128_PAIR) return launch_fwd_pair<128, CAUSAL, VARLEN>(p, stream);
   return launch_fwd_q<D, CAUSAL, VARLEN, FwdCfg<D>::kQT>(p, stream);
 }
 

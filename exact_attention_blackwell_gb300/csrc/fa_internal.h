@@ -35,7 +35,7 @@ struct FwdParams {
   CUtensorMap tm_k;  // [B, N, Hkv, d]
   CUtensorMap tm_v;  // [B, N, Hkv, d]
   CUtensorMap tm_o;  // [B, N, H, d] (store)
-  CUtensorMap tm_k64;  // K in boxes of 64 rows (head-dim-256 CTA-pair kernel)
+  CUtensorMap tm_k64;  // K in boxes of 64 rows (CTA-pair kernels)
   float *lse;        // [B, H, N] or nullptr
   unsigned *status;  // device status word: [0] error bits, [1] failing site, [2] rescale count
   int B, H, Hkv, N;

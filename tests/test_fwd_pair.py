@@ -1,13 +1,14 @@
-"""The head-dim-256 forward on CTA pairs against the one-tile forward.
+"""The CTA-pair forward against the one-CTA forward, at head dims 256 and 128.
 
 At head dim 256 the default library runs the forward on clusters of two CTAs
 that share 256 query rows (128 each): M = 256 `cta_group::2` MMAs, each CTA
-loading half of K_j (64 key rows) and half of V_j (128 head-dim columns), S
-double-buffered in TMEM (FA4 paper summary, section 2.C).  A build with
-FA_FWD256_PAIR=0 keeps one query tile per CTA.  Both must match the oracle on
-shapes whose pair's second tile is empty or ragged, under the causal mask
-(the pair's first tile masks the last key block whole), with GQA, for a
-single row and on packed batches.
+loading half of K_j (64 key rows) and half of V_j (half the head dim), S
+double-buffered in TMEM (FA4 paper summary, section 2.C).  At head dim 128 the
+default keeps two query tiles per CTA (the pair form measured slower there).
+One variant build swaps both (FA_FWD256_PAIR=0, FA_FWD128_PAIR=1).  Every form
+must match the oracle on shapes whose pair's second tile is empty or ragged,
+under the causal mask (the pair's first tile masks the last key block whole),
+with GQA, for a single row and on packed batches.
 """
 import ctypes
 import math
@@ -24,9 +25,9 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 @pytest.fixture(scope="module")
-def one_tile_lib(tmp_path_factory):
-    path = str(tmp_path_factory.mktemp("fwd1") / "libfa_fwd1.so")
-    build.build(force=True, extra_flags=["-DFA_FWD256_PAIR=0"], lib_path=path)
+def variant_lib(tmp_path_factory):
+    path = str(tmp_path_factory.mktemp("fwdv") / "libfa_fwdv.so")
+    build.build(force=True, extra_flags=["-DFA_FWD256_PAIR=0", "-DFA_FWD128_PAIR=1"], lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_fwd", "fa_fwd_varlen", "fa_last_device_status"):
         res, args = fa.SIGNATURES[name]
@@ -45,24 +46,24 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [256, 128])
 @pytest.mark.parametrize("B,N,H,Hkv,causal", CASES)
-def test_pair_and_one_tile_forward_match_oracle(oracle_mod, one_tile_lib, B, N, H, Hkv, causal):
-    d = 256
-    seed = 8100 + N + H + causal
+def test_default_and_variant_forward_match_oracle(oracle_mod, variant_lib, d, B, N, H, Hkv, causal):
+    seed = 8100 + N + H + causal + d
     q = inputs.random_bf16((B, N, H, d), seed, "cuda")
     k = inputs.random_bf16((B, N, Hkv, d), seed + 1, "cuda")
     v = inputs.random_bf16((B, N, Hkv, d), seed + 2, "cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.attention_fwd(q, k, v, scale=scale, causal=causal)
     o1, lse1 = torch.empty_like(q), torch.empty_like(lse)
-    assert one_tile_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), lse1.data_ptr(), B, H, Hkv,
+    assert variant_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), lse1.data_ptr(), B, H, Hkv,
                                N, d, scale, int(causal), None) == fa.FA_OK
     torch.cuda.synchronize()
-    assert one_tile_lib.fa_last_device_status(None) == fa.FA_OK
+    assert variant_lib.fa_last_device_status(None) == fa.FA_OK
     assert fa.fa_last_device_status() == fa.FA_OK
     o_ref, lse_ref = oracle_mod.attention_fwd(q.cpu(), k.cpu(), v.cpu(), scale, causal)
-    what = f"d256 B{B} N{N} H{H}/{Hkv} causal={causal}"
-    for name, oo, ll in (("pair", o, lse), ("one tile", o1, lse1)):
+    what = f"d{d} B{B} N{N} H{H}/{Hkv} causal={causal}"
+    for name, oo, ll in (("default", o, lse), ("variant", o1, lse1)):
         check_o(oo.float().cpu().numpy().astype(np.float64), o_ref, f"{name} {what}")
         check_lse(ll.cpu().numpy().astype(np.float64), lse_ref, f"{name} {what}")
 
