@@ -4,7 +4,7 @@ the workload (default: B=4, H=16, N=8192, d=128, non-causal, bf16), inputs
 resident in HBM, timed with CUDA events.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload headline|causal|gqa]
+                  [--workload headline|causal|gqa|varlen|fp8|sweep-d<64|128|256>-n<1024|4096|16384>[-causal]]
 
 --impl reference times the fp64 CPU oracle (a deliberately slow, plain
 statement of the same computation) on the host cores: each step is the forward
@@ -37,9 +37,18 @@ METRIC = "attention TFLOPs/s fwd & bwd (bf16, d=128) at 1 GB300; fraction of 2.2
 NOMINAL_BF16_TFLOPS = 2250.0
 
 
+def sweep_name(d: int, N: int, causal: bool) -> str:
+    return f"sweep-d{d}-n{N}" + ("-causal" if causal else "")
+
+
+SWEEP_NAMES = [sweep_name(d, N, c) for d in (64, 128, 256) for N in (1024, 4096, 16384) for c in (False, True)]
+
+
 def workload(name: str):
     from exact_attention_blackwell_gb300 import inputs
 
+    if name.startswith("sweep-"):  # one point of the head-dim sweep (B*N = 32768 tokens, H = 16)
+        return {sweep_name(w.d, w.N, w.causal): w for w in inputs.sweep()}[name]
     return {"headline": inputs.headline, "causal": inputs.causal_outliers, "gqa": inputs.long_gqa,
             "varlen": inputs.packed_causal}[name]()
 
@@ -453,9 +462,11 @@ def run_ours(args):
         # executed GEMM flops of each backward kernel: dK/dV recomputes S^T and dP^T
         # (4 GEMMs of 2 N^2 d per head), dQ recomputes S and dP (3 GEMMs)
         gemm = fwd_f / 2  # one N x N x d GEMM pass over all heads, causal halving included
-        dkdv_name = "bwd_dkdv_pair_kernel" if d == 128 else "bwd_dkdv_kernel"  # head dim 128 runs on CTA pairs
+        # head dims 128 and 256 run on CTA pairs
+        dkdv_name = {128: "bwd_dkdv_pair_kernel", 256: "bwd_dkdv256_pair_kernel"}.get(d, "bwd_dkdv_kernel")
+        dq_name = "bwd_dq256_pair_kernel" if d == 256 else "bwd_dq_kernel"
         kern = (dkdv_name, dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
-            ("bwd_dq_kernel", dq_ms, 3 * gemm, "fa_bwd.cu")
+            (dq_name, dq_ms, 3 * gemm, "fa_bwd.cu")
         name, kms, kflops, _ = kern
         src = kernel_source_hash(["fa_bwd.cu", "ptx.cuh", "exp2_poly.cuh", "fa_internal.h"])
         achieved = kflops / (kms * 1e-3) / 1e12
@@ -866,7 +877,8 @@ def main():
                     help="timed steps (default: 100 for our arm, 20 for the CPU oracle arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen", "fp8"], default="headline")
+    ap.add_argument("--workload", choices=["headline", "causal", "gqa", "varlen", "fp8"] + SWEEP_NAMES,
+                    default="headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shard", action="store_true",
