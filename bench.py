@@ -462,8 +462,10 @@ def run_ours(args):
         # executed GEMM flops of each backward kernel: dK/dV recomputes S^T and dP^T
         # (4 GEMMs of 2 N^2 d per head), dQ recomputes S and dP (3 GEMMs)
         gemm = fwd_f / 2  # one N x N x d GEMM pass over all heads, causal halving included
-        # head dims 128 and 256 run on CTA pairs
-        dkdv_name = {128: "bwd_dkdv_pair_kernel", 256: "bwd_dkdv256_pair_kernel"}.get(d, "bwd_dkdv_kernel")
+        # head dim 256 runs on CTA pairs; head dim 128 too for sequences longer than
+        # 2048 rows (4096 causal: FA_DKDV_PAIR_MIN_N[_CAUSAL] in fa_bwd.cu)
+        pair128 = d == 128 and N > (4096 if causal else 2048)
+        dkdv_name = "bwd_dkdv256_pair_kernel" if d == 256 else "bwd_dkdv_pair_kernel" if pair128 else "bwd_dkdv_kernel"
         dq_name = "bwd_dq256_pair_kernel" if d == 256 else "bwd_dq_kernel"
         kern = (dkdv_name, dkdv_ms, 4 * gemm, "fa_bwd.cu") if dkdv_ms >= dq_ms else \
             (dq_name, dq_ms, 3 * gemm, "fa_bwd.cu")

@@ -39,6 +39,19 @@
 #ifndef FA_DKDV_PAIR
 #define FA_DKDV_PAIR 1
 #endif
+// Sequence lengths (the longest one for packed batches) up to which the one-CTA
+// dK/dV kernel runs at head dim 128 even with pairs enabled.  Measured on GB300
+// (back-to-back launches, H = 16, B*N = 32768 unless noted): one CTA faster by
+// 0-7 % non-causal at N <= 2048 and by 3-15 % causal at N <= 4096 (the pair's
+// second key tile spends one iteration on a query tile it masks whole); pairs
+// faster by 2-3 % non-causal at N = 4096, 3-4 % at the B4 N8192 headline shape,
+// 0.5-6 % causal at N = 8192, 2-4 % at N = 16384 and 6 % on B1 H32/8 N32768.
+#ifndef FA_DKDV_PAIR_MIN_N
+#define FA_DKDV_PAIR_MIN_N 2048
+#endif
+#ifndef FA_DKDV_PAIR_MIN_N_CAUSAL
+#define FA_DKDV_PAIR_MIN_N_CAUSAL 4096
+#endif
 // dQ at head dim 128 on CTA pairs (1) or on single CTAs (0, the default).
 #ifndef FA_DQ_PAIR
 #define FA_DQ_PAIR 0
@@ -3553,7 +3566,7 @@ int launch_bwd_dkdv(const BwdParams &p, int d, bool causal, cudaStream_t stream)
   switch (d) {
     case 64: return causal ? launch_dkdv_t<64, true>(p, stream) : launch_dkdv_t<64, false>(p, stream);
     case 128:
-      if (FA_DKDV_PAIR)
+      if (FA_DKDV_PAIR && p.N > (causal ? FA_DKDV_PAIR_MIN_N_CAUSAL : FA_DKDV_PAIR_MIN_N))
         return causal ? launch_dkdv_pair_t<true>(p, stream) : launch_dkdv_pair_t<false>(p, stream);
       return causal ? launch_dkdv_t<128, true>(p, stream) : launch_dkdv_t<128, false>(p, stream);
     case 256: {

@@ -2,12 +2,14 @@
 
 At head dim 128 the default library computes dK and dV with cluster pairs of
 CTAs sharing one 256-row key tile, each M = 256 MMA reading half of its B
-operand from each CTA (FlashAttention-4 paper summary, section 2.C).  A build
-with FA_DKDV_PAIR=0 keeps the one-CTA kernel; both must match the oracle, and
-they must give bitwise equal dK and dV on shapes whose last
-key tile has no partner (odd tile counts), whose partner lies wholly past the
-end of the sequence, under the causal mask (the pair's second tile sees a
-query tile that it must mask whole) and with GQA.
+operand from each CTA (FlashAttention-4 paper summary, section 2.C), for
+sequences longer than 2048 rows (4096 causal); shorter ones run the one-CTA
+kernel, measured faster there.  The tests below use short shapes, so the
+default library runs the one-CTA kernel and a build with both thresholds at 0
+runs the pair; both must match the oracle, and they must give bitwise equal dK
+and dV on shapes whose last key tile has no partner (odd tile counts), whose
+partner lies wholly past the end of the sequence, under the causal mask (the
+pair's second tile sees a query tile that it must mask whole) and with GQA.
 """
 import ctypes
 import math
@@ -22,10 +24,13 @@ from helpers import check_grad
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
+PAIR_ALWAYS = ["-DFA_DKDV_PAIR_MIN_N=0", "-DFA_DKDV_PAIR_MIN_N_CAUSAL=0"]
+
+
 @pytest.fixture(scope="module")
-def single_cta_lib(tmp_path_factory):
-    path = str(tmp_path_factory.mktemp("single") / "libfa_dkdv1.so")
-    build.build(force=True, extra_flags=["-DFA_DKDV_PAIR=0"], lib_path=path)
+def pair_lib(tmp_path_factory):
+    path = str(tmp_path_factory.mktemp("pair") / "libfa_dkdv2.so")
+    build.build(force=True, extra_flags=PAIR_ALWAYS, lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_last_device_status"):
         res, args = fa.SIGNATURES[name]
@@ -45,7 +50,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("B,N,H,Hkv,causal", CASES)
-def test_pair_and_single_cta_dkdv_agree_and_match_oracle(oracle_mod, single_cta_lib, B, N, H, Hkv, causal):
+def test_pair_and_single_cta_dkdv_agree_and_match_oracle(oracle_mod, pair_lib, B, N, H, Hkv, causal):
     d = 128
     seed = 7100 + N + H + causal
     q = inputs.random_bf16((B, N, H, d), seed, "cuda")
@@ -54,16 +59,16 @@ def test_pair_and_single_cta_dkdv_agree_and_match_oracle(oracle_mod, single_cta_
     dO = inputs.random_bf16((B, N, H, d), seed + 3, "cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.attention_fwd(q, k, v, scale=scale, causal=causal)
-    pair = fa.attention_bwd(q, k, v, o, lse, dO, scale=scale, causal=causal)
-    nb = single_cta_lib.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
+    one = fa.attention_bwd(q, k, v, o, lse, dO, scale=scale, causal=causal)  # short: the one-CTA kernel
+    nb = pair_lib.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-    one = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
-    st = single_cta_lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
-                               one[0].data_ptr(), one[1].data_ptr(), one[2].data_ptr(), B, H, Hkv, N, d, scale,
-                               int(causal), ws.data_ptr(), nb, None)
+    pair = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    st = pair_lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+                         pair[0].data_ptr(), pair[1].data_ptr(), pair[2].data_ptr(), B, H, Hkv, N, d, scale,
+                         int(causal), ws.data_ptr(), nb, None)
     assert st == fa.FA_OK
     torch.cuda.synchronize()
-    assert single_cta_lib.fa_last_device_status(None) == fa.FA_OK
+    assert pair_lib.fa_last_device_status(None) == fa.FA_OK
     assert fa.fa_last_device_status() == fa.FA_OK
     ref = oracle_mod.attention_bwd(q.cpu(), k.cpu(), v.cpu(), dO.cpu(), scale, causal)
     what = f"B{B} N{N} H{H}/{Hkv} causal={causal}"
@@ -78,7 +83,7 @@ def test_pair_and_single_cta_dkdv_agree_and_match_oracle(oracle_mod, single_cta_
 @pytest.fixture(scope="module")
 def cluster_scope_lib(tmp_path_factory):
     path = str(tmp_path_factory.mktemp("clscope") / "libfa_clscope.so")
-    build.build(force=True, extra_flags=["-DFA_PAIR_SCOPE_CLUSTER=1"], lib_path=path)
+    build.build(force=True, extra_flags=["-DFA_PAIR_SCOPE_CLUSTER=1"] + PAIR_ALWAYS, lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_last_device_status"):
         res, args = fa.SIGNATURES[name]
@@ -99,6 +104,7 @@ def test_cluster_scope_build_gives_the_same_bits(cluster_scope_lib, B, N, H, Hkv
     dO = inputs.random_bf16((B, N, H, d), seed + 3, "cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.attention_fwd(q, k, v, scale=scale, causal=causal)
+    # the default library runs the one-CTA kernel at these lengths, bitwise equal to the pair
     ref = fa.attention_bwd(q, k, v, o, lse, dO, scale=scale, causal=causal)
     nb = cluster_scope_lib.fa_bwd_workspace_bytes(B, H, Hkv, N, d)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
