@@ -253,6 +253,24 @@ def profiled_traffic(summary: str, src_hash: str):
     return float(m_b.group(1))
 
 
+def oracle_tiny_one_thread() -> float:
+    """Seconds of one fwd + bwd of the tiny case (B1 H2 N128 d64) by the oracle on one thread."""
+    import oracle
+    from exact_attention_blackwell_gb300 import inputs
+
+    w = inputs.tiny()
+    x = inputs.make_inputs(w)
+    all_threads = oracle.num_threads()
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.attention_fwd(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
+        oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], w.sm_scale, w.causal)
+        return time.perf_counter() - t0
+    finally:
+        oracle.set_threads(all_threads)
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 def cpu_oracle_step(x, w, head: int):
     """fwd + bwd of one (b, h) slice with the fp64 oracle; returns seconds."""
@@ -577,7 +595,9 @@ def run_ours(args):
 
         oracle.build()
         t = cpu_oracle_step(x_cpu, w, 0)
+        tiny_1t = oracle_tiny_one_thread()
         out["cpu_baseline"] = {"value": head_flops(w) / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                               "tiny_one_thread_seconds": tiny_1t,
                                "kind": "oracle", "seconds": t,
                                "sample": f"(batch 0, head 0) slice: {N} query rows x {N} keys, d={d}, "
                                          f"{'fwd+bwd' if w.backward else 'fwd'}, fp64",

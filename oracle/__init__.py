@@ -54,6 +54,8 @@ def _load():
         lib.oracle_bwd_rows.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
         _lib = lib
     return _lib
 
@@ -85,6 +87,11 @@ def _rows(rows, N):
 def num_threads() -> int:
     """OpenMP threads one oracle call uses."""
     return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Sets the OpenMP threads of later oracle calls (timing only; results do not depend on it)."""
+    _load().oracle_set_threads(int(n))
 
 
 def attention_fwd(q, k, v, scale: float, causal: bool, rows=None):

@@ -221,6 +221,15 @@ void oracle_bwd(const double *q, const double *k, const double *v, const double 
   oracle_bwd_rows(q, k, v, dO, B, H, Hkv, N, d, scale, causal, NULL, N, NULL, N, dq, dk, dv);
 }
 
+/* Threads for this library's later parallel regions (n >= 1); for timing only. */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Number of OpenMP threads a parallel region of this library uses. */
 int oracle_num_threads(void) {
   int n = 1;

@@ -288,3 +288,23 @@ def test_varlen_sequences_do_not_see_each_other(oracle_mod):
     for a, b in zip(g1, g2):
         np.testing.assert_array_equal(a[:5], b[:5])
     assert not np.allclose(o1[5:], o2[5:])
+
+
+def test_oracle_results_do_not_depend_on_its_thread_count(oracle_mod):
+    # rows are split across OpenMP threads, each computed in a fixed order: the
+    # one-thread run the CPU baseline times gives the same numbers
+    q, k, v = qkv(1, 128, 2, 2, 64, 4400)
+    dO = rnd((1, 128, 2, 64), 4404)
+    scale = 1.0 / math.sqrt(64)
+    full = oracle_mod.attention_fwd(q, k, v, scale, False)
+    grads = oracle_mod.attention_bwd(q, k, v, dO, scale, False)
+    n = oracle_mod.num_threads()
+    oracle_mod.set_threads(1)
+    try:
+        assert oracle_mod.num_threads() == 1
+        one = oracle_mod.attention_fwd(q, k, v, scale, False)
+        grads1 = oracle_mod.attention_bwd(q, k, v, dO, scale, False)
+    finally:
+        oracle_mod.set_threads(n)
+    for a, b in zip(full + tuple(grads), one + tuple(grads1)):
+        assert np.array_equal(a, b)
