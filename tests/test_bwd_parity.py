@@ -71,6 +71,12 @@ CASES = [
     (1, 256, 2, 2, 256, False),
     (1, 333, 2, 1, 256, True),
     (2, 128, 2, 2, 256, True),
+    # either side of the lengths where head-dim-128 dK/dV moves from one CTA per
+    # key tile to CTA pairs (2048 rows, 4096 causal); the longer ones are ragged
+    (1, 2048, 2, 2, 128, False),
+    (1, 2049, 2, 1, 128, False),
+    (1, 4096, 1, 1, 128, True),
+    (1, 4097, 1, 1, 128, True),
 ]
 
 
