@@ -105,3 +105,39 @@ def test_head_dim_sweep(oracle_mod, w):
     rows = sample_rows(w.N, 192, w.seed)
     check_sampled(oracle_mod, w, x, got, groups=[(0, 0), (w.B - 1, w.H - 1)], rows=rows,
                   grad_rows=rows if w.N > 4096 else None)
+
+
+def test_packed_workload_full_size(oracle_mod):
+    """The packed batch bench.py --workload varlen times (65536 tokens, 128..16384-row
+    sequences, H16 d128 causal), computed whole; the oracle recomputes sampled rows of
+    the shortest, a middle and the longest sequence for the first and last heads."""
+    w = inputs.packed_causal()
+    x = inputs.make_packed_inputs(w)
+    q, k, v, dO = (x[n].cuda() for n in ("q", "k", "v", "dO"))
+    cu = x["cu_seqlens"].cuda()
+    o, lse = fa.attention_fwd_varlen(q, k, v, cu, w.max_seqlen, scale=w.sm_scale, causal=w.causal)
+    dq, dk, dv = fa.attention_bwd_varlen(q, k, v, o, lse, dO, cu, w.max_seqlen, scale=w.sm_scale, causal=w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse, dq, dk, dv = (t.cpu() for t in (o, lse, dq, dk, dv))
+    bounds = w.cu_seqlens()
+    lens = list(w.lens)
+    order = sorted(range(len(lens)), key=lambda b: lens[b])
+    for b in (order[0], order[len(order) // 2], order[-1]):
+        a, e = bounds[b], bounds[b + 1]
+        L = e - a
+        rows = sample_rows(L, 96, w.seed + b)
+        for h in (0, w.H - 1):
+            kh = h // (w.H // w.Hkv)
+            sl = lambda t, hh: t[a:e, hh:hh + 1][None]  # one sequence, one head: [1, L, 1, d]
+            what = f"packed seq {b} ({L} rows) head {h}"
+            o_ref, lse_ref = oracle_mod.attention_fwd(sl(x["q"], h), sl(x["k"], kh), sl(x["v"], kh), w.sm_scale,
+                                                      w.causal, rows=rows)
+            check_o(o[a:e][rows, h:h + 1][None].float().numpy().astype(np.float64), o_ref, what)
+            check_lse(lse[h, a:e][rows][None, None].numpy().astype(np.float64), lse_ref, what)
+            rq, rk, rv = oracle_mod.attention_bwd(sl(x["q"], h), sl(x["k"], kh), sl(x["v"], kh), sl(x["dO"], h),
+                                                  w.sm_scale, w.causal, qrows=rows, kvrows=rows)
+            check_grad(dq[a:e][rows, h:h + 1][None], rq, what + " dQ")
+            if w.H == w.Hkv:  # dK, dV of a kv head sum over its query heads: compare only 1:1 heads
+                check_grad(dk[a:e][rows, kh:kh + 1][None], rk, what + " dK")
+                check_grad(dv[a:e][rows, kh:kh + 1][None], rv, what + " dV")
