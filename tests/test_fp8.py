@@ -128,3 +128,32 @@ def test_rotation_lowers_the_error_on_outlier_inputs(oracle_mod):
                         np.sqrt(np.mean((lse.cpu().numpy() - l_ex) ** 2)))
     assert errs[True][0] * 1.2 <= errs[False][0], errs
     assert errs[True][1] * 1.3 <= errs[False][1], errs
+
+
+@pytest.mark.slow
+def test_headline_shape_full_size(oracle_mod):
+    """The shape bench.py --workload fp8 times (B4 H16 N8192 d128), computed whole; the
+    oracle checks sampled rows of the first and last (batch, head) slices.  The oracle's
+    scales are per head (and per 128-row block of Q and K), so quantizing one head's
+    slice gives exactly the values the whole tensors would."""
+    B, N, H, Hkv = 4, 8192, 16, 16
+    w, x, s, o, lse, ws = run(B, N, H, Hkv, False, 8400)
+    sgn = s.numpy().astype(np.float64)
+    rng = np.random.default_rng(8401)
+    rows = np.array(sorted(set(rng.choice(N, 126, replace=False).tolist()) | {0, N - 1}), dtype=np.int32)
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy()
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = lambda t: t[b:b + 1, :, h:h + 1]
+        qh, kh, vh = fp8_ref.attention_fwd_fp8_inputs(sl(x["q"]), sl(x["k"]), sl(x["v"]), sgn)
+        o_ref, lse_ref = oracle_mod.attention_fwd(qh, kh, vh, w.sm_scale, False, rows=rows)
+        o_abs, _ = oracle_mod.attention_fwd(qh, kh, np.abs(vh), w.sm_scale, False, rows=rows)
+        what = f"fp8 headline b{b} h{h}"
+        check_lse(lse[b:b + 1, h:h + 1][:, :, rows], lse_ref, what)
+        got = o[b:b + 1, rows, h:h + 1]
+        bound = 2.0 ** -4 * o_abs + 4 * 2.0 ** -10 / math.sqrt(3) * math.sqrt(N) * np.abs(vh).max() + \
+            half_ulp_bf16(o_ref) + 1e-3
+        err = np.abs(got - o_ref)
+        assert (err <= bound).all(), f"{what}: worst excess {(err - bound).max():.3e}"
+        rel = np.linalg.norm(got - o_ref) / np.linalg.norm(o_ref)
+        assert rel <= 2.0 ** -5, f"{what}: relative RMS error {rel:.3e}"
