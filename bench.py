@@ -471,11 +471,15 @@ def run_ours(args):
            "config": dict(config_of(w), input_sha256=inputs.input_sha256(x_cpu)[:16]),
            "frac_of_2250_tflops": value / world / NOMINAL_BF16_TFLOPS,
            "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms}
+    # the metric's own flop counts (backward = 2.5 x forward) against the measured burst peak:
+    # unlike roofline.frac (executed flops of one kernel) these charge the recomputed GEMMs
+    out["fwd_frac_of_burst"] = out["fwd_tflops"] / peaks["burst"]
     if w.backward:
         dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev)
         dq_ms = statistics.mean(a.elapsed_time(b) for a, b in dq_ev)
         out["bwd_ms"] = ms_step - fwd_ms
         out["bwd_tflops"] = bwd_f / ((ms_step - fwd_ms) * 1e-3) / 1e12
+        out["bwd_frac_of_burst"] = out["bwd_tflops"] / peaks["burst"]
         out["dkdv_ms"], out["dq_ms"] = dkdv_ms, dq_ms
         # executed GEMM flops of each backward kernel: dK/dV recomputes S^T and dP^T
         # (4 GEMMs of 2 N^2 d per head), dQ recomputes S and dP (3 GEMMs)
