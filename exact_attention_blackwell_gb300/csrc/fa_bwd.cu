@@ -327,8 +327,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
   const int wg = warp >> 2;            // query columns [QW wg, QW wg + QW)
   const int r = threadIdx.x & 127;     // key row within the tile == TMEM lane
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t s_tm = tmem + lane_off + C::kColS + QW * wg;  // S^T columns of this warpgroup
-  const uint32_t p_tm = s_tm;                                  // P^T (bf16) over their first QW / 2
+  const uint32_t s_tm0 = tmem + lane_off + C::kColS + QW * wg;  // S^T columns of this warpgroup (buffer 0)
   const uint32_t dp_tm = tmem + lane_off + C::kColDP + QW * wg;
   const uint32_t ds_tm = dp_tm;                                // dS^T (bf16) over the first QW / 2 dP^T columns
   const bool row_valid = kv0 + r < L;  // key rows past the sequence: P = 0
@@ -340,7 +339,10 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
     const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + QW * wg;
     const float *dlt_s = lse2_s + 128;
     // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
-    ok = wait_warp(bar(C::kBarS), it & 1, kBSiteS);
+    const int sb = it % C::kSBufs;  // S^T buffer of this iteration
+    const uint32_t s_tm = s_tm0 + 128u * sb;
+    const uint32_t p_tm = s_tm;  // P^T (bf16) over the first QW / 2 of the S^T columns
+    ok = wait_warp(bar(C::kBarS + sb), (it / C::kSBufs) & 1, kBSiteS);
     if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
@@ -361,7 +363,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
       dkdv_p<false, QW>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     tmem_wait_st();
     tc_fence_before();
-    if (!(FA_STALL(2) && it == 0)) signal_mma(C::kBarP);
+    if (!(FA_STALL(2) && it == 0)) signal_mma(C::kBarP + sb);
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
     // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
     ok = wait_warp(bar(C::kBarDP), it & 1, kBSiteDP);
@@ -431,7 +433,11 @@ struct DkdvCfg {
   static constexpr int kNumWG = 2;
   static constexpr int kThreads = 32 * (4 * kNumWG + 2);
   static constexpr int kMmaWarp = 4 * kNumWG, kLoadWarp = 4 * kNumWG + 1;
-  static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // S^T buffers: at head dim 64 TMEM holds two, so S^T_{i+2} is computed while
+  // the elementwise warps work on iteration i and they never wait for S^T; at
+  // 128 the accumulators leave room for one.
+  static constexpr int kSBufs = (D == 64) ? 2 : 1;
+  static constexpr int kColS = 0, kColDP = 128 * kSBufs, kColDV = kColDP + 128, kColDK = kColDV + D;
   static constexpr int kTmemCols = 512;
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
   static constexpr int kOffK = 0;
@@ -439,8 +445,8 @@ struct DkdvCfg {
   static constexpr int kOffRing = 2 * kTile;
   static constexpr int kOffRows = kOffRing + kSlots * kTile;  // row stage r: LSE2 at +1024r, D at +1024r+512
   enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
-         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages, kBarDP, kBarP, kBarDS,
-         kBarFinal, kBarDrain, kNumBars };
+         kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages,  // S, P: one per S^T buffer
+         kBarDP = kBarS + kSBufs, kBarP, kBarDS = kBarP + kSBufs, kBarFinal, kBarDrain, kNumBars };
   static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked in the kernel)
@@ -481,7 +487,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
-      const bool all = i == C::kBarP || i == C::kBarDS || (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
+      const bool all = (i >= C::kBarP && i < C::kBarP + C::kSBufs) || i == C::kBarDS ||
+                       (i >= C::kBarRowEmpty0 && i < C::kBarRowEmpty0 + C::kRowStages);
       mbar_init(bar(i), all ? (uint32_t)(4 * C::kNumWG) : 1u);  // one arrival per elementwise warp
     }
     *abort_flag = 0;
@@ -542,11 +549,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
-    // Order: S_0 dP_0 | [P_0] dV_0 S_1 [dS_0] dK_0 dP_1 | [P_1] dV_1 S_2 [dS_1] dK_1 dP_2 | ...
+    // Order (one S^T buffer): S_0 dP_0 | [P_0] dV_0 S_1 [dS_0] dK_0 dP_1 | [P_1] dV_1 S_2 [dS_1] dK_1 dP_2 | ...
     // P^T_i (S^T columns) is read by dV_i, which precedes S_{i+1}; dS^T_i (dP^T
     // columns) is read by dK_i, which precedes dP_{i+1}: the tensor pipe runs
     // one thread's MMAs in order.  The elementwise warps have loaded S^T_i and
-    // dP^T_i into registers before they signal P_i and dS_i.
+    // dP^T_i into registers before they signal P_i and dS_i.  With two S^T
+    // buffers S runs one iteration further ahead: S_0 S_1 dP_0 | [P_0] dV_0 S_2
+    // [dS_0] dK_0 dP_1 | ..., S_{i+2} overwriting buffer i % 2 after dV_i.
     // The whole warp runs the loop and waits; the elected lane issues.
     {
       constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -561,12 +570,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
       auto full_ok = [&](int fill) {
         return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), C::phase(fill), wctx, kBSiteFull);
       };
-      auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it)
+      auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it) into buffer it % kSBufs
+        const int sb = it % C::kSBufs;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColS, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
-          tc_commit(bar(C::kBarS));
+            mma_ss(tmem + C::kColS + 128u * sb, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
+          tc_commit(bar(C::kBarS + sb));
         }
         __syncwarp();
       };
@@ -589,7 +599,14 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
         tc_fence_after();
         issue_s(0);
         if (lane == 0) FA_LIFE(0, 3);
-        ok = full_ok(1);
+        if (C::kSBufs == 2 && n_iter > 1) {
+          ok = full_ok(2);
+          if (ok) {
+            tc_fence_after();
+            issue_s(1);
+          }
+        }
+        if (ok) ok = full_ok(1);
       }
       if (ok) {
         tc_fence_after();
@@ -597,8 +614,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
       }
       for (int it = 0; it < n_iter && ok; ++it) {
         const bool more = it + 1 < n_iter;
+        const int sb = it % C::kSBufs;
         FA_TRACE_EV(0, it, 8);
-        ok = mbar_wait_warp(bar(C::kBarP), it & 1, wctx, kBSiteP);
+        ok = mbar_wait_warp(bar(C::kBarP + sb), (it / C::kSBufs) & 1, wctx, kBSiteP);
         if (!ok) break;
         FA_TRACE_EV(0, it, 9);
         tc_fence_after();
@@ -606,18 +624,18 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + a_col(kk), ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128),
-                   id_dv, (it > 0 || kk > 0));
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + 128u * sb + a_col(kk),
+                   ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128), id_dv, (it > 0 || kk > 0));
           tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
         }
         __syncwarp();
-        if (more) {
+        if (it + C::kSBufs < n_iter) {  // S^T of iteration it + kSBufs, over P^T_it's buffer
           FA_TRACE_EV(0, it, 12);
-          ok = full_ok(2 * it + 2);
+          ok = full_ok(2 * (it + C::kSBufs));
           if (!ok) break;
           FA_TRACE_EV(0, it, 13);
           tc_fence_after();
-          issue_s(it + 1);
+          issue_s(it + C::kSBufs);
         }
         ok = mbar_wait_warp(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
         if (!ok) break;
@@ -2176,6 +2194,7 @@ struct Dkdv256Cfg {
   static constexpr int kNumWG = 2;
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
+  static constexpr int kSBufs = 1;  // one S^T buffer (the elementwise rows are shared with the other kernels)
   static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
   static constexpr int kTmemCols = 512;
   static constexpr int kOffK = 0, kOffV = kTile, kOffRing = 2 * kTile;
