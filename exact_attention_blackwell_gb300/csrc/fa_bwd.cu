@@ -1528,10 +1528,12 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
   const int wg = warp >> 2;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t s_tm = tmem + lane_off + C::kColS + KW * wg;
-  const uint32_t dp_tm = tmem + lane_off + C::kColDP + KW * wg;
-  const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first KW / 2 of this warpgroup's dP columns
+  const uint32_t dp_tm0 = tmem + lane_off + C::kColDP + KW * wg;  // dP columns of this warpgroup (buffer 0)
   bool ok = true;
   for (int j = 0; j < nb && ok; ++j) {
+    const int db = j % C::kDPBufs;  // dP buffer of this key tile
+    const uint32_t dp_tm = dp_tm0 + 128u * db;
+    const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first KW / 2 of this warpgroup's dP columns
     ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
@@ -1560,7 +1562,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
       for (int c = 0; c < KW; ++c)
         if (c > lim) pe[c] = 0.f;
     }
-    ok = mbar_wait_warp(bar(C::kBarDP), j & 1, wctx, kBSiteDP);
+    ok = mbar_wait_warp(bar(C::kBarDP + db), (j / C::kDPBufs) & 1, wctx, kBSiteDP);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 1);
     tc_fence_after();
@@ -1584,7 +1586,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
       tmem_st_32x32b_x16(ds_tm, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
     tmem_wait_st();
     tc_fence_before();
-    if (!(FA_STALL(3) && j == 0)) signal_mma(C::kBarDS);
+    if (!(FA_STALL(3) && j == 0)) signal_mma(C::kBarDS + db);
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
   }
   return ok;
@@ -1617,14 +1619,17 @@ struct DqCfg {
   static constexpr int kMmaWarp = 4 * kNumWG, kLoadWarp = 4 * kNumWG + 1;
   // TMEM: S (fp32), dP (fp32; dS bf16 over it once read), dQ (fp32), and the
   // CTA's Q and dO tiles (bf16, two per column) as A operands of the S and dP MMAs.
-  static constexpr int kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
+  // At head dim 64 dP has two buffers, so dP_{j+1} can be issued before dS_j
+  // is ready (it overwrites dS_{j-1}, which dQ_{j-1} read earlier in issue order).
+  static constexpr int kDPBufs = (D == 64) ? 2 : 1;
+  static constexpr int kColS = 0, kColDP = 128, kColDQ = 128 + 128 * kDPBufs, kColQ = kColDQ + D, kColDO = kColQ + D / 2;
   static constexpr int kTmemCols = 512;
   static_assert(kColDO + D / 2 <= kTmemCols, "TMEM budget");
   static constexpr int kOffRing = 0;
   static constexpr int kOffStage = 0;  // dQ epilogue staging: ring slot 0, drained by then
   static constexpr int kOffBar = kOffRing + kStages * kTile;
   enum { kBarQdo, kBarFull0, kBarEmpty0 = kBarFull0 + kStages, kBarS = kBarEmpty0 + kStages, kBarSFree, kBarDP,
-         kBarDS, kBarFinal, kBarDrain, kNumBars };
+         kBarDS = kBarDP + kDPBufs, kBarFinal = kBarDS + kDPBufs, kBarDrain, kNumBars };  // DP, DS: one per dP buffer
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -1662,7 +1667,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
       // per elementwise warp: Q and dO come from the first two warpgroups only
-      mbar_init(bar(i), i == C::kBarQdo ? 8u : (i == C::kBarSFree || i == C::kBarDS) ? (uint32_t)(4 * C::kNumWG) : 1u);
+      mbar_init(bar(i), i == C::kBarQdo ? 8u
+                        : (i == C::kBarSFree || (i >= C::kBarDS && i < C::kBarDS + C::kDPBufs)) ? (uint32_t)(4 * C::kNumWG)
+                                                                                                  : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1748,8 +1755,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
     // Order: S_0 dP_0 | [S read] S_{j+1} [dS_j] dQ_j dP_{j+1} | ...
     // S_{j+1} overwrites S_j once the elementwise warps hold it in registers;
     // dS_j (bf16, over the dP columns) is read by dQ_j, which precedes dP_{j+1}
-    // (the tensor pipe runs one thread's MMAs in order).  The whole warp runs
-    // the loop and waits; the elected lane issues.
+    // (the tensor pipe runs one thread's MMAs in order).  With two dP buffers
+    // the order is S_{j+1} dP_{j+1} [dS_j] dQ_j: dP_{j+1} goes to the buffer of
+    // dS_{j-1}, whose dQ_{j-1} was issued before it.  The whole warp runs the
+    // loop and waits; the elected lane issues.
     {
       constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP (A in TMEM, B K-major)
       constexpr uint32_t id_dq = make_idesc_bf16(128, D, false, true);    // dQ (A = dS in TMEM, B = K MN-major)
@@ -1773,13 +1782,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
         }
         __syncwarp();
       };
-      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
+      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T, into buffer j % kDPBufs
+        const int db = j % C::kDPBufs;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColDP, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj(kk), id_s,
-                   kk > 0);
-          tc_commit(bar(C::kBarDP));
+            mma_ts(tmem + C::kColDP + 128u * db, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj(kk),
+                   id_s, kk > 0);
+          tc_commit(bar(C::kBarDP + db));
           tc_commit(bar(C::kBarEmpty0 + C::slot(fv(j))));  // V_j consumed
         }
         __syncwarp();
@@ -1813,8 +1823,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
           FA_TRACE_EV(1, j, 13);
           tc_fence_after();
           issue_s(j + 1);
+          if (C::kDPBufs == 2) {
+            ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(j + 1);
+          }
         }
-        ok = mbar_wait_warp(bar(C::kBarDS), j & 1, wctx, kBSiteDS);
+        const int db = j % C::kDPBufs;
+        ok = mbar_wait_warp(bar(C::kBarDS + db), (j / C::kDPBufs) & 1, wctx, kBSiteDS);
         if (!ok) break;
         FA_TRACE_EV(1, j, 9);
         tc_fence_after();
@@ -1822,12 +1839,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + a_col(kk), ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128),
-                   id_dq, (j > 0 || kk > 0));
+            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + 128u * db + a_col(kk),
+                   ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
           tc_commit(bar(C::kBarEmpty0 + C::slot(fk(j))));  // K_j consumed
         }
         __syncwarp();
-        if (more) {
+        if (C::kDPBufs == 1 && more) {
           ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
           if (!ok) break;
           tc_fence_after();
@@ -2905,6 +2922,7 @@ struct Dq256Cfg {
   static constexpr int kNumWG = 2;
   static constexpr int kThreads = 320;
   static constexpr int kMmaWarp = 8;  // warp 9: TMA producer
+  static constexpr int kDPBufs = 1;
   static constexpr int kColS = 0, kColDP = 128, kColDQ = 256;
   static constexpr int kTmemCols = 512;
   static constexpr int kOffQ = 0, kOffDO = kTile, kOffRing = 2 * kTile;
