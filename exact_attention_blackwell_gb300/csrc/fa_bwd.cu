@@ -52,6 +52,17 @@
 #ifndef FA_DKDV_PAIR_MIN_N_CAUSAL
 #define FA_DKDV_PAIR_MIN_N_CAUSAL 4096
 #endif
+// Head-dim-64 dK/dV: persistent CTAs (one per SM, each running a strided
+// share of the work units) for sequences up to this many rows; longer ones get
+// one CTA per unit, scheduled by the hardware.  Causal: the persistent kernel
+// carries a few spilled registers, which cost more than the set-up it saves
+// once a unit runs tens of iterations.
+#ifndef FA_DKDV_PERSIST_MAX_N
+#define FA_DKDV_PERSIST_MAX_N (1 << 30)
+#endif
+#ifndef FA_DKDV_PERSIST_MAX_N_CAUSAL
+#define FA_DKDV_PERSIST_MAX_N_CAUSAL 8192
+#endif
 // dQ at head dim 128 on CTA pairs (1) or on single CTAs (0, the default).
 #ifndef FA_DQ_PAIR
 #define FA_DQ_PAIR 0
@@ -310,10 +321,12 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&sv)[QW / 32][32], float 
 // runs as a CTA pair whose rank-0 CTA issues the MMAs; the P and dS signals go
 // to that CTA's barriers and every wait has cluster scope.  Returns false if a
 // wait ran out.
+// git0: iterations the CTA ran before this work unit (rings and barrier phases
+// count across units).
 template <class C, bool CAUSAL, bool PAIR = false>
 __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *smem, uint32_t bar0, uint32_t tmem,
                                           const WaitCtx &wctx, int warp, int n_iter, int i_start, int per_head,
-                                          int jt, int kv0, int L) {
+                                          int jt, int kv0, int L, int git0 = 0) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
   auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
     return PAIR ? mbar_wait_warp_cl(b, parity, wctx, site) : mbar_wait_warp(b, parity, wctx, site);
@@ -334,16 +347,17 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
   const bool warp_has_invalid = __any_sync(0xffffffffu, !row_valid);
   bool ok = true;
   for (int it = 0; it < n_iter && ok; ++it) {
-    const int rs = it % C::kRowStages;
+    const unsigned gi = (unsigned)(git0 + it);  // iteration count over the CTA's units
+    const int rs = gi % C::kRowStages;
     const int i = i_start + it % per_head;
     const float *lse2_s = reinterpret_cast<const float *>(smem + C::kOffRows + 1024 * rs) + QW * wg;
     const float *dlt_s = lse2_s + 128;
     // ---- P^T = 2^(S^T c - LSE2), masked; bf16 into TMEM over S^T
-    const int sb = it % C::kSBufs;  // S^T buffer of this iteration
+    const int sb = gi % C::kSBufs;  // S^T buffer of this iteration
     const uint32_t s_tm = s_tm0 + 128u * sb;
     const uint32_t p_tm = s_tm;  // P^T (bf16) over the first QW / 2 of the S^T columns
-    ok = wait_warp(bar(C::kBarS + sb), (it / C::kSBufs) & 1, kBSiteS);
-    if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (it / C::kRowStages) & 1, wctx, kBSiteFull);
+    ok = wait_warp(bar(C::kBarS + sb), (gi / C::kSBufs) & 1, kBSiteS);
+    if (ok) ok = mbar_wait_warp(bar(C::kBarRowFull0 + rs), (gi / C::kRowStages) & 1, wctx, kBSiteFull);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 0);
     tc_fence_after();
@@ -363,10 +377,10 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
       dkdv_p<false, QW>(sv, pe, lse2_s, p.scale_log2, wg, r, row_valid, diag, qoff, p_tm);
     tmem_wait_st();
     tc_fence_before();
-    if (!(FA_STALL(2) && it == 0)) signal_mma(C::kBarP + sb);
+    if (!(FA_STALL(2) && gi == 0)) signal_mma(C::kBarP + sb);
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 1);
     // ---- dS^T = P^T (dP^T - D) -> TMEM (bf16) over the dP^T columns just read
-    ok = wait_warp(bar(C::kBarDP), it & 1, kBSiteDP);
+    ok = wait_warp(bar(C::kBarDP), gi & 1, kBSiteDP);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(0, it, 2);
     tc_fence_after();
@@ -402,7 +416,7 @@ __device__ __forceinline__ bool dkdv_rows(const BwdParams &p, const uint8_t *sme
 }
 
 // ================================================================== dK, dV
-template <int D>
+template <int D, bool PERSIST = false>
 struct DkdvCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128-row bf16 tile
   // Q_i and dO_i stream through a ring of single-tile slots (Q_i = fill 2i,
@@ -415,14 +429,15 @@ struct DkdvCfg {
   // of two iterations back and left it short of its latency.)
   static constexpr int kQSlots = (3 * kSlots + 4) / 5;  // 5 -> 3, 10 -> 6
   static constexpr int kDoSlots = kSlots - kQSlots;
-  // fill 2 i = Q_i, fill 2 i + 1 = dO_i
+  // fill 2 i = Q_i, fill 2 i + 1 = dO_i (fills count up from 0: unsigned
+  // arithmetic, no sign fix-ups on the MMA warp's handoff path)
   __device__ static int slot(int fill) {
-    const int i = fill >> 1;
-    return (fill & 1) ? kQSlots + i % kDoSlots : i % kQSlots;
+    const unsigned i = (unsigned)fill >> 1;
+    return (int)((fill & 1) ? kQSlots + i % kDoSlots : i % kQSlots);
   }
   __device__ static uint32_t phase(int fill) {
-    const int i = fill >> 1;
-    return (uint32_t)(((fill & 1) ? i / kDoSlots : i / kQSlots) & 1);
+    const unsigned i = (unsigned)fill >> 1;
+    return ((fill & 1) ? i / kDoSlots : i / kQSlots) & 1u;
   }
   static constexpr int kRowStages = 2;  // own full/empty barriers, released after each dS
   // Elementwise warpgroups (thread = key row, a warpgroup per 128 / kNumWG query
@@ -440,22 +455,65 @@ struct DkdvCfg {
   static constexpr int kColS = 0, kColDP = 128 * kSBufs, kColDV = kColDP + 128, kColDK = kColDV + D;
   static constexpr int kTmemCols = 512;
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
+  // PERSIST (head dim 64 only, for the shared-memory budget): the grid is at
+  // most one CTA per SM and each CTA runs work units blockIdx.x, blockIdx.x +
+  // gridDim.x, ...; the dK/dV epilogue then stages through a region of its
+  // own, since the ring already holds the next unit's Q and dO.  With one unit
+  // per CTA the staging reuses ring slots 0 and 1, drained once every MMA has
+  // completed.
+  static constexpr bool kPersist = PERSIST;
+  static_assert(!PERSIST || D == 64, "persistent dK/dV CTAs: head dim 64 only");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
   static constexpr int kOffRing = 2 * kTile;
   static constexpr int kOffRows = kOffRing + kSlots * kTile;  // row stage r: LSE2 at +1024r, D at +1024r+512
+  static constexpr int kOffStage = kPersist ? kOffRows + 1024 * kRowStages : kOffRing;  // dV, then dK at +kTile
   enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
          kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages,  // S, P: one per S^T buffer
-         kBarDP = kBarS + kSBufs, kBarP, kBarDS = kBarP + kSBufs, kBarFinal, kBarDrain, kNumBars };
-  static constexpr int kOffBar = kOffRows + 1024 * kRowStages;
+         kBarDP = kBarS + kSBufs, kBarP, kBarDS = kBarP + kSBufs, kBarFinal, kBarDrain,
+         kBarKVFree,  // the unit's last S^T and dP^T have read K and V
+         kNumBars };
+  static constexpr int kOffBar = kPersist ? kOffStage + 2 * kTile : kOffRows + 1024 * kRowStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked in the kernel)
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-  using C = DkdvCfg<D>;
+// One work unit of the one-CTA dK/dV kernel: key tile jt of one (batch, kv head).
+struct DkdvUnit {
+  SeqSpan sq;
+  int b, jt, kh, kv0, n_iter, i_start, per_head;
+  bool skip;  // packed batch: the tile lies past its sequence, no rows to produce
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ DkdvUnit dkdv_unit(const BwdParams &p, int u) {
+  DkdvUnit w;
+  int rank, head;
+  work_order(u, (p.N + 127) / 128, p.B * p.Hkv, p.sched_chunk, rank, head);
+  w.jt = rank;  // causal: tile 0 sees the most query tiles
+  w.kh = head % p.Hkv;
+  w.b = head / p.Hkv;
+  w.sq = VARLEN ? seq_span(p.cu_seqlens, w.b, p.N, p.total) : SeqSpan{0, p.N, w.b};
+  w.kv0 = w.jt * 128;
+  w.skip = VARLEN && w.kv0 >= w.sq.len;
+  const int n_q = (w.sq.len + 127) / 128;
+  w.i_start = CAUSAL ? w.jt : 0;
+  w.per_head = n_q - w.i_start;
+  w.n_iter = (p.H / p.Hkv) * w.per_head;  // (head, query tile) pairs, head-major; >= 1 unless skip
+  return w;
+}
+
+// The CTA runs work units blockIdx.x, blockIdx.x + gridDim.x, ... (one per CTA
+// at head dim 128, where the grid covers every unit).  The roles go from one
+// unit into the next without a block-wide barrier: every ring, S^T buffer and
+// barrier phase counts iterations over the CTA's units, the producer loads the
+// next unit's K and V once the last MMA reading this unit's has completed
+// (kBarKVFree), and the next unit's first S^T and dP^T overlap this unit's
+// last elementwise step and epilogue.
+template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
+__global__ void __launch_bounds__(DkdvCfg<D, PERSIST>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = DkdvCfg<D, PERSIST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (!check_align(sbase, p.status)) return;
@@ -469,21 +527,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_kv = (p.N + 127) / 128;
-  int rank, head;
-  work_order((int)blockIdx.x, n_kv, p.B * p.Hkv, p.sched_chunk, rank, head);
-  const int jt = rank;  // key/value tile; causal: tile 0 sees the most query tiles
-  const int kh = head % p.Hkv, b = head / p.Hkv;
   const int g = p.H / p.Hkv;
-  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
-  const int L = sq.len;  // rows of this sequence
   const int Npad = (p.N + 127) / 128 * 128;  // row-term arrays are [B, H, Npad]
-  const int kv0 = jt * 128;
-  if (VARLEN && kv0 >= L) return;  // the tile lies past its sequence: no rows to produce
-  const int n_q = (L + 127) / 128;
-  const int i_start = CAUSAL ? jt : 0;
-  const int per_head = n_q - i_start;
-  const int n_iter = g * per_head;  // (head, query tile) pairs, head-major
+  const int n_units = (p.N + 127) / 128 * p.B * p.Hkv;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i) {
@@ -499,9 +545,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
     tmem_relinquish();
   }
   if (warp == C::kLoadWarp && lane == 0) {
-    prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
+    prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_do);
   }
   tc_fence_before();
@@ -514,38 +560,57 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
     // ===================================================== P^T and dS^T, one warpgroup per 128 / kNumWG query columns
     // P stays in registers (fp32) from its computation to dS; P^T (bf16) goes
     // to TMEM over the S^T columns for the dV MMA, dS^T (bf16) over the dP^T
-    // columns once they have been read, for the dK MMA.
+    // columns once they have been read, for the dK MMA.  After a wait has run
+    // out these warps still step through every unit (doing nothing but the
+    // epilogue's named barrier), so both warpgroups' barriers stay matched.
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, n_iter, i_start, per_head, jt, kv0, L);
-    // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale (via ring slots 0 and 1,
-    //      drained once every MMA has completed); any further warpgroups are done
-    if (wg < 2) {
-    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
-    if (threadIdx.x == 0) FA_LIFE(0, 4);
-    tc_fence_after();
-    uint8_t *stage = smem + C::kOffRing + wg * C::kTile;
-    const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
-    const float mul = wg == 0 ? 1.0f : p.scale;
-    const bool direct = VARLEN && kv0 + 128 > L;  // the next sequence's rows follow: write row by row
-    if (ok && direct) {
-      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
-      acc_to_global<D>(acc_tm, out + ((size_t)(sq.start + kv0 + r) * p.Hkv + kh) * D, 0, mul, kv0 + r < L);
-    } else if (ok) {
-      acc_to_smem<D>(acc_tm, stage, r, 0, mul);
-    }
-    fence_proxy_async_smem();
-    if (wg == 0) named_bar_sync(1, 128);
-    else named_bar_sync(2, 128);
-    if (r == 0 && ok && !direct) {
-      const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
-      for (int bx = 0; bx < D / 64; ++bx)
-        tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, kh, sq.start + kv0, sq.bc);
-      bulk_commit();
-      bulk_wait_read_all();
-      if (threadIdx.x == 0) FA_LIFE(0, 5);
-    }
+    bool ok = true;
+    int git = 0, uc = 0;  // iterations and units this CTA has run
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const DkdvUnit w = dkdv_unit<CAUSAL, VARLEN>(p, u);
+      if (w.skip) continue;
+      if (ok)
+        ok = dkdv_rows<C, CAUSAL>(p, smem, bar0, tmem, wctx, warp, w.n_iter, w.i_start, w.per_head, w.jt, w.kv0,
+                                  w.sq.len, git);
+      git += w.n_iter;
+      // ---- epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK * scale; any further warpgroups are done.
+      // The stage is free: its previous TMA store was read out before warp 0 of
+      // the warpgroup signalled this unit's first P^T, which every MMA of the unit follows.
+      if (wg < 2) {
+        // the unit's coordinates again, from a copy of u the compiler cannot
+        // match to the first: only u stays live across the iterations
+        const DkdvUnit w = dkdv_unit<CAUSAL, VARLEN>(p, C::kPersist ? __shfl_sync(0xffffffffu, u, 0) : u);
+        if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), uc & 1, wctx, kBSiteFinal);
+        if (threadIdx.x == 0) FA_LIFE(0, 4);
+        tc_fence_after();
+        uint8_t *stage = smem + C::kOffStage + wg * C::kTile;
+        const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
+        const float mul = wg == 0 ? 1.0f : p.scale;
+        const bool direct = VARLEN && w.kv0 + 128 > w.sq.len;  // the next sequence's rows follow: write row by row
+        if (ok && direct) {
+          __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
+          acc_to_global<D>(acc_tm, out + ((size_t)(w.sq.start + w.kv0 + r) * p.Hkv + w.kh) * D, 0, mul,
+                           w.kv0 + r < w.sq.len);
+        } else if (ok) {
+          acc_to_smem<D>(acc_tm, stage, r, 0, mul);
+        }
+        tc_fence_before();  // the accumulator reads precede the next unit's first dV / dK MMA
+        fence_proxy_async_smem();
+        if (wg == 0) named_bar_sync(1, 128);
+        else named_bar_sync(2, 128);
+        if (r == 0 && ok && !direct) {
+          const CUtensorMap *map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_store_4d(map, smem_u32(stage) + bx * 16384, bx * 64, w.kh, w.sq.start + w.kv0, w.sq.bc);
+          bulk_commit();
+          bulk_wait_read_all();
+          if (threadIdx.x == 0) FA_LIFE(0, 5);
+        }
+      }
+      ++uc;
+      if (!C::kPersist) break;  // one unit per CTA
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
@@ -556,6 +621,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
     // dP^T_i into registers before they signal P_i and dS_i.  With two S^T
     // buffers S runs one iteration further ahead: S_0 S_1 dP_0 | [P_0] dV_0 S_2
     // [dS_0] dK_0 dP_1 | ..., S_{i+2} overwriting buffer i % 2 after dV_i.
+    // Indices count over the CTA's units; a unit's first S and dP wait for its
+    // K and V, and its first dV and dK (which overwrite the accumulators) follow
+    // its first P and dS, signalled after the previous epilogue read them.
     // The whole warp runs the loop and waits; the elected lane issues.
     {
       constexpr uint32_t id_kk = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -570,22 +638,23 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
       auto full_ok = [&](int fill) {
         return mbar_wait_warp(bar(C::kBarFull0 + slot_of(fill)), C::phase(fill), wctx, kBSiteFull);
       };
-      auto issue_s = [&](int it) {  // S^T = K Q^T   (Q_it is fill 2 it) into buffer it % kSBufs
-        const int sb = it % C::kSBufs;
+      auto issue_s = [&](unsigned gi) {  // S^T = K Q^T   (Q_gi is fill 2 gi) into buffer gi % kSBufs
+        const unsigned sb = gi % C::kSBufs;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColS + 128u * sb, k_d + kmaj(kk), ring_d + soff(2 * it) + kmaj(kk), id_kk, kk > 0);
+            mma_ss(tmem + C::kColS + 128u * sb, k_d + kmaj(kk), ring_d + soff(2 * gi) + kmaj(kk), id_kk, kk > 0);
           tc_commit(bar(C::kBarS + sb));
         }
         __syncwarp();
       };
-      auto issue_dp = [&](int it) {  // dP^T = V dO^T   (dO_it is fill 2 it + 1)
+      auto issue_dp = [&](unsigned gi, bool last) {  // dP^T = V dO^T   (dO_gi is fill 2 gi + 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * it + 1) + kmaj(kk), id_kk, kk > 0);
+            mma_ss(tmem + C::kColDP, v_d + kmaj(kk), ring_d + soff(2 * gi + 1) + kmaj(kk), id_kk, kk > 0);
           tc_commit(bar(C::kBarDP));
+          if (C::kPersist && last) tc_commit(bar(C::kBarKVFree));  // the unit's last MMA reading K or V
         }
         __syncwarp();
       };
@@ -593,75 +662,85 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
       // QW w of the region, in bf16 pairs; 16 query rows per K step = 8 columns.
       constexpr int QW = 128 / C::kNumWG, KPW = QW / 16;  // query columns and 16-row K steps per warpgroup
       auto a_col = [](int kk) { return (uint32_t)(QW * (kk / KPW) + 8 * (kk % KPW)); };
-      bool ok = mbar_wait_warp(bar(C::kBarKV), 0, wctx, kBSiteKV);
-      if (ok) ok = full_ok(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        if (lane == 0) FA_LIFE(0, 3);
-        if (C::kSBufs == 2 && n_iter > 1) {
-          ok = full_ok(2);
-          if (ok) {
-            tc_fence_after();
-            issue_s(1);
+      bool ok = true;
+      int git = 0, uc = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DkdvUnit w = dkdv_unit<CAUSAL, VARLEN>(p, u);
+        if (w.skip) continue;
+        const int n_iter = w.n_iter, G = git;
+        ok = mbar_wait_warp(bar(C::kBarKV), uc & 1, wctx, kBSiteKV);
+        if (ok) ok = full_ok(2 * G);
+        if (ok) {
+          tc_fence_after();
+          issue_s(G);
+          if (uc == 0 && lane == 0) FA_LIFE(0, 3);
+          if (C::kSBufs == 2 && n_iter > 1) {
+            ok = full_ok(2 * (G + 1));
+            if (ok) {
+              tc_fence_after();
+              issue_s(G + 1);
+            }
           }
+          if (ok) ok = full_ok(2 * G + 1);
         }
-        if (ok) ok = full_ok(1);
-      }
-      if (ok) {
-        tc_fence_after();
-        issue_dp(0);
-      }
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const bool more = it + 1 < n_iter;
-        const int sb = it % C::kSBufs;
-        FA_TRACE_EV(0, it, 8);
-        ok = mbar_wait_warp(bar(C::kBarP + sb), (it / C::kSBufs) & 1, wctx, kBSiteP);
-        if (!ok) break;
-        FA_TRACE_EV(0, it, 9);
-        tc_fence_after();
-        // dV += P^T dO_it
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + 128u * sb + a_col(kk),
-                   ring_mn + soff(2 * it + 1) + (uint64_t)(kk * 128), id_dv, (it > 0 || kk > 0));
-          tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it + 1)));  // dO_it consumed (dP_it, dV_it)
-        }
-        __syncwarp();
-        if (it + C::kSBufs < n_iter) {  // S^T of iteration it + kSBufs, over P^T_it's buffer
-          FA_TRACE_EV(0, it, 12);
-          ok = full_ok(2 * (it + C::kSBufs));
-          if (!ok) break;
-          FA_TRACE_EV(0, it, 13);
+        if (ok) {
           tc_fence_after();
-          issue_s(it + C::kSBufs);
+          issue_dp(G, n_iter == 1);
         }
-        ok = mbar_wait_warp(bar(C::kBarDS), it & 1, wctx, kBSiteDS);
-        if (!ok) break;
-        FA_TRACE_EV(0, it, 10);
-        tc_fence_after();
-        // dK += dS^T Q_it
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * it) + (uint64_t)(kk * 128),
-                   id_dv, (it > 0 || kk > 0));
-          tc_commit(bar(C::kBarEmpty0 + slot_of(2 * it)));  // Q_it consumed (S_it, dK_it)
-        }
-        __syncwarp();
-        if (more) {
-          ok = full_ok(2 * it + 3);
+        for (int it = 0; it < n_iter && ok; ++it) {
+          const unsigned gi = (unsigned)(G + it);
+          const bool more = it + 1 < n_iter;
+          const unsigned sb = gi % C::kSBufs;
+          FA_TRACE_EV(0, it, 8);
+          ok = mbar_wait_warp(bar(C::kBarP + sb), (gi / C::kSBufs) & 1, wctx, kBSiteP);
           if (!ok) break;
+          FA_TRACE_EV(0, it, 9);
           tc_fence_after();
-          issue_dp(it + 1);
+          // dV += P^T dO_gi
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::kColDV, tmem + C::kColS + 128u * sb + a_col(kk),
+                     ring_mn + soff(2 * gi + 1) + (uint64_t)(kk * 128), id_dv, (it > 0 || kk > 0));
+            tc_commit(bar(C::kBarEmpty0 + slot_of(2 * gi + 1)));  // dO_gi consumed (dP_gi, dV_gi)
+          }
+          __syncwarp();
+          if (it + C::kSBufs < n_iter) {  // S^T of iteration gi + kSBufs, over P^T_gi's buffer
+            FA_TRACE_EV(0, it, 12);
+            ok = full_ok(2 * (gi + C::kSBufs));
+            if (!ok) break;
+            FA_TRACE_EV(0, it, 13);
+            tc_fence_after();
+            issue_s(gi + C::kSBufs);
+          }
+          ok = mbar_wait_warp(bar(C::kBarDS), gi & 1, wctx, kBSiteDS);
+          if (!ok) break;
+          FA_TRACE_EV(0, it, 10);
+          tc_fence_after();
+          // dK += dS^T Q_gi
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::kColDK, tmem + C::kColDP + a_col(kk), ring_mn + soff(2 * gi) + (uint64_t)(kk * 128),
+                     id_dv, (it > 0 || kk > 0));
+            tc_commit(bar(C::kBarEmpty0 + slot_of(2 * gi)));  // Q_gi consumed (S_gi, dK_gi)
+          }
+          __syncwarp();
+          if (more) {
+            ok = full_ok(2 * gi + 3);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp(gi + 1, it + 2 == n_iter);
+          }
+          FA_TRACE_EV(0, it, 11);
         }
-        FA_TRACE_EV(0, it, 11);
+        if (elect_one()) tc_commit(bar(C::kBarFinal));  // the unit's accumulators are complete
+        __syncwarp();
+        git += n_iter;
+        ++uc;
+        if (!C::kPersist) break;
       }
-      if (elect_one()) {
-        tc_commit(bar(C::kBarFinal));
-        tc_commit(bar(C::kBarDrain));
-      }
+      if (elect_one()) tc_commit(bar(C::kBarDrain));
       __syncwarp();
       if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
@@ -672,42 +751,55 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
     // ===================================================== TMA producer
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();  // Q, dO, LSE2, D are re-read by every key tile
-      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTile);
-      for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
-        tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, kh, sq.start + kv0, sq.bc);
-      }
       bool ok = true;
-      int fill = 0, rows_issued = 0;
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int hh = kh * g + it / per_head;
-        const int i = i_start + it % per_head;
-        for (int t = 0; t < 2 && ok; ++t, ++fill) {  // t = 0: Q_it, t = 1: dO_it
-          const int s = C::slot(fill);
-          ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
-          if (!ok) break;
-          const uint32_t fb = bar(C::kBarFull0 + s);
-          mbar_arrive_expect_tx(fb, C::kTile);
-          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
-          for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, sq.start + i * 128, sq.bc,
-                             keep);
-          FA_TRACE_EV(0, it, 4 + t);
+      int fill = 0, rows_issued = 0, git = 0, uc = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DkdvUnit w = dkdv_unit<CAUSAL, VARLEN>(p, u);
+        if (w.skip) continue;
+        // K and V of this unit, once the previous unit's last S^T and dP^T have read theirs
+        if (uc > 0) ok = mbar_wait(bar(C::kBarKVFree), (uc - 1) & 1, wctx, kBSiteEmpty);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTile);
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_4d(sbase + C::kOffK + bx * 16384, &p.tm_k, bar(C::kBarKV), bx * 64, w.kh, w.sq.start + w.kv0,
+                      w.sq.bc);
+          tma_load_4d(sbase + C::kOffV + bx * 16384, &p.tm_v, bar(C::kBarKV), bx * 64, w.kh, w.sq.start + w.kv0,
+                      w.sq.bc);
         }
-        if (!ok) break;
-        // LSE2 / D rows of iteration it, into row stage it % kRowStages once the
-        // elementwise warps are done with iteration it - kRowStages
-        const int rs = it % C::kRowStages;
-        ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((it / C::kRowStages) & 1) ^ 1, wctx, kBSiteEmpty);
-        if (!ok) break;
-        const uint32_t rb = bar(C::kBarRowFull0 + rs);
-        mbar_arrive_expect_tx(rb, 1024);
-        const size_t roff = ((size_t)b * p.H + hh) * Npad + (size_t)i * 128;
-        const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
-        bulk_load(rdst, p.lse2 + roff, 512, rb);
-        bulk_load(rdst + 512, p.delta + roff, 512, rb);
-        FA_TRACE_EV(0, it, 6);
-        ++rows_issued;
+        for (int it = 0; it < w.n_iter && ok; ++it) {
+          const unsigned gi = (unsigned)(git + it);
+          const int hh = w.kh * g + it / w.per_head;
+          const int i = w.i_start + it % w.per_head;
+          for (int t = 0; t < 2 && ok; ++t, ++fill) {  // t = 0: Q_gi, t = 1: dO_gi
+            const int s = C::slot(fill);
+            ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
+            if (!ok) break;
+            const uint32_t fb = bar(C::kBarFull0 + s);
+            mbar_arrive_expect_tx(fb, C::kTile);
+            const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_load_4d_hint(dst + bx * 16384, t == 0 ? &p.tm_q : &p.tm_do, fb, bx * 64, hh, w.sq.start + i * 128,
+                               w.sq.bc, keep);
+            FA_TRACE_EV(0, it, 4 + t);
+          }
+          if (!ok) break;
+          // LSE2 / D rows of iteration gi, into row stage gi % kRowStages once the
+          // elementwise warps are done with iteration gi - kRowStages
+          const unsigned rs = gi % C::kRowStages;
+          ok = mbar_wait(bar(C::kBarRowEmpty0 + rs), ((gi / C::kRowStages) & 1u) ^ 1u, wctx, kBSiteEmpty);
+          if (!ok) break;
+          const uint32_t rb = bar(C::kBarRowFull0 + rs);
+          mbar_arrive_expect_tx(rb, 1024);
+          const size_t roff = ((size_t)w.b * p.H + hh) * Npad + (size_t)i * 128;
+          const uint32_t rdst = sbase + C::kOffRows + 1024 * rs;
+          bulk_load(rdst, p.lse2 + roff, 512, rb);
+          bulk_load(rdst + 512, p.delta + roff, 512, rb);
+          FA_TRACE_EV(0, it, 6);
+          ++rows_issued;
+        }
+        git += w.n_iter;
+        ++uc;
+        if (!C::kPersist) break;
       }
       const uint64_t t0 = global_timer_ns();
       // the last issued fill of each slot: Q_i for the last kQSlots i issued, dO_i for the last kDoSlots
@@ -721,7 +813,9 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1) bwd_dkdv_kernel(const
       for (int f = max(0, rows_issued - C::kRowStages); f < rows_issued; ++f)
         while (!mbar_test(bar(C::kBarRowFull0 + f % C::kRowStages), (f / C::kRowStages) & 1) &&
                global_timer_ns() - t0 < kWaitLimitNs) {}
-      while (!mbar_test(bar(C::kBarKV), 0) && global_timer_ns() - t0 < kWaitLimitNs) {}
+      // the last K / V load issued (unit uc - 1; a load is issued for every unit counted)
+      if (uc > 0)
+        while (!mbar_test(bar(C::kBarKV), (uc - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
     }
   }
 
@@ -3527,15 +3621,33 @@ unsigned grid_1d(long long n_tiles, long long n_heads) {
   return n > 0x7fffffffLL ? 0u : (unsigned)n;  // 0: too many CTAs for a 1-D grid
 }
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
 template <int D, bool CAUSAL>
 int launch_dkdv_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_kv_order(p_in, CAUSAL, D);
-  const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.Hkv);
+  unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.Hkv);
   if (!grid) return FA_ERR_UNSUPPORTED;
+  if constexpr (D == 64) {
+    if (p.N <= (CAUSAL ? FA_DKDV_PERSIST_MAX_N_CAUSAL : FA_DKDV_PERSIST_MAX_N)) {  // at most one CTA per SM
+      using PC = DkdvCfg<D, true>;
+      const int sms = sm_count();
+      if (sms > 0 && grid > (unsigned)sms) grid = (unsigned)sms;
+      return p.cu_seqlens ? launch_kernel(bwd_dkdv_kernel<D, CAUSAL, true, true>, dim3(grid), PC::kThreads,
+                                          PC::kSmemBytes, p, stream)
+                          : launch_kernel(bwd_dkdv_kernel<D, CAUSAL, false, true>, dim3(grid), PC::kThreads,
+                                          PC::kSmemBytes, p, stream);
+    }
+  }
   return p.cu_seqlens
-             ? launch_kernel(bwd_dkdv_kernel<D, CAUSAL, true>, dim3(grid), DkdvCfg<D>::kThreads, DkdvCfg<D>::kSmemBytes,
-                             p, stream)
-             : launch_kernel(bwd_dkdv_kernel<D, CAUSAL, false>, dim3(grid), DkdvCfg<D>::kThreads,
+             ? launch_kernel(bwd_dkdv_kernel<D, CAUSAL, true, false>, dim3(grid), DkdvCfg<D>::kThreads,
+                             DkdvCfg<D>::kSmemBytes, p, stream)
+             : launch_kernel(bwd_dkdv_kernel<D, CAUSAL, false, false>, dim3(grid), DkdvCfg<D>::kThreads,
                              DkdvCfg<D>::kSmemBytes, p, stream);
 }
 

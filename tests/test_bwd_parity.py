@@ -68,6 +68,9 @@ CASES = [
     (1, 256, 2, 2, 64, False),
     (1, 395, 2, 2, 64, True),
     (2, 200, 4, 2, 64, True),
+    # more head-dim-64 key tiles than SMs: persistent dK/dV CTAs run several units
+    (8, 333, 16, 8, 64, True),
+    (4, 640, 8, 8, 64, False),
     (1, 256, 2, 2, 256, False),
     (1, 333, 2, 1, 256, True),
     (2, 128, 2, 2, 256, True),

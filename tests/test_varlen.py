@@ -92,6 +92,9 @@ BWD_CASES = [
     ([5, 200, 64, 385], 2, 2, 64, True),
     ([333, 17, 256], 2, 1, 256, True),
     ([333, 17, 256], 2, 2, 256, False),
+    # 40 sequences of 0-299 rows at head dim 64: 240 key-tile units, many past
+    # their sequence, on persistent dK/dV CTAs that each run several
+    ([(37 * i * i + 11 * i) % 300 for i in range(40)], 4, 2, 64, True),
 ]
 
 

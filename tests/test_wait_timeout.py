@@ -67,10 +67,17 @@ def test_default_build_has_no_stall_hook():
     assert fa.lib().fa_debug_stall(1) == fa.FA_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("mode,causal", [(1, True), (2, True), (2, False), (3, True)])
-def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(oracle_mod, stall_lib, mode, causal):
-    B, H, N, d = 1, 2, 640, 128
-    w = inputs.Workload("stall", B, H, H, N, d, causal, 6100 + mode)
+# (mode, causal, B, H, d).  At head dim 64 the dK/dV kernel is persistent: with
+# 320 work units on at most one CTA per SM, block 0 runs several, and after the
+# stall in its first unit it must step through the rest and still return.
+CASES = [(1, True, 1, 2, 128), (2, True, 1, 2, 128), (2, False, 1, 2, 128), (3, True, 1, 2, 128),
+         (2, True, 4, 16, 64), (2, False, 4, 16, 64)]
+
+
+@pytest.mark.parametrize("mode,causal,B,H,d", CASES)
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct(oracle_mod, stall_lib, mode, causal, B, H, d):
+    N = 640
+    w = inputs.Workload("stall", B, H, H, N, d, causal, 6100 + mode + d)
     x = inputs.make_inputs(w, device="cuda")
     site = ctypes.c_int(-1)
     assert stall_lib.fa_last_device_status_site(None, ctypes.byref(site)) == fa.FA_OK and site.value == 0
