@@ -63,6 +63,14 @@
 #ifndef FA_DKDV_PERSIST_MAX_N_CAUSAL
 #define FA_DKDV_PERSIST_MAX_N_CAUSAL 8192
 #endif
+// The same at head dim 128, where the one-CTA kernel runs up to FA_DKDV_PAIR_MIN_N
+// (_CAUSAL) rows; at causal 4096 rows the two forms measured the same.
+#ifndef FA_DKDV128_PERSIST_MAX_N
+#define FA_DKDV128_PERSIST_MAX_N (1 << 30)
+#endif
+#ifndef FA_DKDV128_PERSIST_MAX_N_CAUSAL
+#define FA_DKDV128_PERSIST_MAX_N_CAUSAL 2048
+#endif
 // dQ at head dim 128 on CTA pairs (1) or on single CTAs (0, the default).
 #ifndef FA_DQ_PAIR
 #define FA_DQ_PAIR 0
@@ -230,7 +238,8 @@ __device__ __forceinline__ void acc_to_smem(uint32_t tm_row, uint8_t *stage, int
 
 // The same epilogue for one row straight to global memory (bf16 row `dst`,
 // columns [c0, c0 + NCOLS)): used for the rows of a varlen tile that belong to
-// its sequence when the tile runs past the sequence's end.
+// its sequence when the tile runs past the sequence's end, and by the
+// persistent head-dim-128 dK/dV kernel, which has no room for a stage.
 template <int NCOLS>
 __device__ __forceinline__ void acc_to_global(uint32_t tm_row, __nv_bfloat16 *dst, int c0, float mul, bool write) {
 #pragma unroll
@@ -455,25 +464,27 @@ struct DkdvCfg {
   static constexpr int kColS = 0, kColDP = 128 * kSBufs, kColDV = kColDP + 128, kColDK = kColDV + D;
   static constexpr int kTmemCols = 512;
   static_assert(kColDK + D <= kTmemCols, "TMEM budget");
-  // PERSIST (head dim 64 only, for the shared-memory budget): the grid is at
-  // most one CTA per SM and each CTA runs work units blockIdx.x, blockIdx.x +
-  // gridDim.x, ...; the dK/dV epilogue then stages through a region of its
-  // own, since the ring already holds the next unit's Q and dO.  With one unit
+  // PERSIST: the grid is at most one CTA per SM and each CTA runs work units
+  // blockIdx.x, blockIdx.x + gridDim.x, ...; the ring then already holds the
+  // next unit's Q and dO when the dK/dV epilogue runs, so at head dim 64 the
+  // epilogue stages through a region of its own and at 128 (no room for one)
+  // each thread writes its key row to global memory directly.  With one unit
   // per CTA the staging reuses ring slots 0 and 1, drained once every MMA has
   // completed.
   static constexpr bool kPersist = PERSIST;
-  static_assert(!PERSIST || D == 64, "persistent dK/dV CTAs: head dim 64 only");
+  static constexpr bool kOwnStage = PERSIST && D == 64, kDirectStore = PERSIST && D == 128;
+  static_assert(!PERSIST || D <= 128, "persistent dK/dV CTAs: head dim 64 or 128");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
   static constexpr int kOffRing = 2 * kTile;
   static constexpr int kOffRows = kOffRing + kSlots * kTile;  // row stage r: LSE2 at +1024r, D at +1024r+512
-  static constexpr int kOffStage = kPersist ? kOffRows + 1024 * kRowStages : kOffRing;  // dV, then dK at +kTile
+  static constexpr int kOffStage = kOwnStage ? kOffRows + 1024 * kRowStages : kOffRing;  // dV, then dK at +kTile
   enum { kBarKV, kBarFull0, kBarEmpty0 = kBarFull0 + kSlots, kBarRowFull0 = kBarEmpty0 + kSlots,
          kBarRowEmpty0 = kBarRowFull0 + kRowStages, kBarS = kBarRowEmpty0 + kRowStages,  // S, P: one per S^T buffer
          kBarDP = kBarS + kSBufs, kBarP, kBarDS = kBarP + kSBufs, kBarFinal, kBarDrain,
          kBarKVFree,  // the unit's last S^T and dP^T have read K and V
          kNumBars };
-  static constexpr int kOffBar = kPersist ? kOffStage + 2 * kTile : kOffRows + 1024 * kRowStages;
+  static constexpr int kOffBar = kOwnStage ? kOffStage + 2 * kTile : kOffRows + 1024 * kRowStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kOffMisc + 16;  // base must be 1024-aligned (checked in the kernel)
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -588,11 +599,13 @@ __global__ void __launch_bounds__(DkdvCfg<D, PERSIST>::kThreads, 1) bwd_dkdv_ker
         uint8_t *stage = smem + C::kOffStage + wg * C::kTile;
         const uint32_t acc_tm = tmem + lane_off + (wg == 0 ? C::kColDV : C::kColDK);
         const float mul = wg == 0 ? 1.0f : p.scale;
-        const bool direct = VARLEN && w.kv0 + 128 > w.sq.len;  // the next sequence's rows follow: write row by row
+        // row by row: no stage (persistent, head dim 128), or the next sequence's rows follow
+        const bool direct = C::kDirectStore || (VARLEN && w.kv0 + 128 > w.sq.len);
         if (ok && direct) {
           __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(wg == 0 ? p.dv : p.dk);
-          acc_to_global<D>(acc_tm, out + ((size_t)(w.sq.start + w.kv0 + r) * p.Hkv + w.kh) * D, 0, mul,
-                           w.kv0 + r < w.sq.len);
+          // first row of the sequence: packed batches start at sq.start, fixed-length ones at b N
+          const size_t row0 = VARLEN ? (size_t)w.sq.start : (size_t)w.b * p.N;
+          acc_to_global<D>(acc_tm, out + ((row0 + w.kv0 + r) * p.Hkv + w.kh) * D, 0, mul, w.kv0 + r < w.sq.len);
         } else if (ok) {
           acc_to_smem<D>(acc_tm, stage, r, 0, mul);
         }
@@ -3633,8 +3646,10 @@ int launch_dkdv_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_kv_order(p_in, CAUSAL, D);
   unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.Hkv);
   if (!grid) return FA_ERR_UNSUPPORTED;
-  if constexpr (D == 64) {
-    if (p.N <= (CAUSAL ? FA_DKDV_PERSIST_MAX_N_CAUSAL : FA_DKDV_PERSIST_MAX_N)) {  // at most one CTA per SM
+  if constexpr (D == 64 || D == 128) {
+    const int max_n = D == 64 ? (CAUSAL ? FA_DKDV_PERSIST_MAX_N_CAUSAL : FA_DKDV_PERSIST_MAX_N)
+                              : (CAUSAL ? FA_DKDV128_PERSIST_MAX_N_CAUSAL : FA_DKDV128_PERSIST_MAX_N);
+    if (p.N <= max_n) {  // at most one CTA per SM
       using PC = DkdvCfg<D, true>;
       const int sms = sm_count();
       if (sms > 0 && grid > (unsigned)sms) grid = (unsigned)sms;

@@ -1,11 +1,13 @@
-"""Persistent head-dim-64 dK/dV CTAs against one CTA per key tile.
+"""Persistent dK/dV CTAs against one CTA per key tile, at head dims 64 and 128.
 
-At head dim 64 the default library runs the dK/dV kernel on at most one CTA
-per SM, each taking key-tile units blockIdx.x, blockIdx.x + gridDim.x, ... and
-carrying its rings, TMEM buffers and barrier phases from one unit into the
-next (the next unit's K and V load as soon as the last MMA that read the
-previous ones completes).  Causal sequences longer than 8192 rows run one CTA
-per unit instead.  A build with both thresholds at 0 runs every shape one CTA
+The default library runs the one-CTA dK/dV kernel (head dim 64, and 128 up to
+the lengths where the CTA pairs take over) on at most one CTA per SM, each
+taking key-tile units blockIdx.x, blockIdx.x + gridDim.x, ... and carrying its
+rings, TMEM buffers and barrier phases from one unit into the next (the next
+unit's K and V load as soon as the last MMA that read the previous ones
+completes); at head dim 128 its epilogue writes each key row straight to
+global memory.  Causal head-dim-64 sequences longer than 8192 rows run one CTA
+per unit instead.  A build with every threshold at 0 runs every shape one CTA
 per unit.  Both must match the oracle, and they must give bitwise equal
 gradients: each unit's MMAs see the same bf16 operands in the same order
 whichever CTA runs it.  The shapes give block 0 several units (more units than
@@ -29,7 +31,8 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 @pytest.fixture(scope="module")
 def one_lib(tmp_path_factory):
     path = str(tmp_path_factory.mktemp("onecta") / "libfa_dkdv1.so")
-    build.build(force=True, extra_flags=["-DFA_DKDV_PERSIST_MAX_N=0", "-DFA_DKDV_PERSIST_MAX_N_CAUSAL=0"],
+    build.build(force=True, extra_flags=["-DFA_DKDV_PERSIST_MAX_N=0", "-DFA_DKDV_PERSIST_MAX_N_CAUSAL=0",
+                                         "-DFA_DKDV128_PERSIST_MAX_N=0", "-DFA_DKDV128_PERSIST_MAX_N_CAUSAL=0"],
                 lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_last_device_status"):
@@ -48,10 +51,10 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,N,H,Hkv,causal", CASES)
-def test_persistent_and_one_cta_dkdv_agree_and_match_oracle(oracle_mod, one_lib, B, N, H, Hkv, causal):
-    d = 64
-    seed = 7300 + N + H + causal
+def test_persistent_and_one_cta_dkdv_agree_and_match_oracle(oracle_mod, one_lib, B, N, H, Hkv, causal, d):
+    seed = 7300 + N + H + causal + d
     q = inputs.random_bf16((B, N, H, d), seed, "cuda")
     k = inputs.random_bf16((B, N, Hkv, d), seed + 1, "cuda")
     v = inputs.random_bf16((B, N, Hkv, d), seed + 2, "cuda")
@@ -77,14 +80,15 @@ def test_persistent_and_one_cta_dkdv_agree_and_match_oracle(oracle_mod, one_lib,
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{what} {name}: persistent and one-CTA differ"
 
 
-def test_persistent_packed_batch_matches_one_cta(oracle_mod, one_lib):
+@pytest.mark.parametrize("d,causal", [(64, True), (128, True), (128, False)])
+def test_persistent_packed_batch_matches_one_cta(oracle_mod, one_lib, d, causal):
     lens = [(37 * i * i + 11 * i) % 300 for i in range(40)]  # 0-276 rows: 240 units, many past their sequence
-    H, Hkv, d, causal = 4, 2, 64, True
+    H, Hkv = 4, 2
     total = sum(lens)
-    q = inputs.random_bf16((total, H, d), 7400, "cuda")
-    k = inputs.random_bf16((total, Hkv, d), 7401, "cuda")
-    v = inputs.random_bf16((total, Hkv, d), 7402, "cuda")
-    dO = inputs.random_bf16((total, H, d), 7403, "cuda")
+    q = inputs.random_bf16((total, H, d), 7400 + d, "cuda")
+    k = inputs.random_bf16((total, Hkv, d), 7401 + d, "cuda")
+    v = inputs.random_bf16((total, Hkv, d), 7402 + d, "cuda")
+    dO = inputs.random_bf16((total, H, d), 7403 + d, "cuda")
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = fa.attention_fwd_varlen(q, k, v, cu, max(lens), scale=scale, causal=causal)
@@ -101,5 +105,6 @@ def test_persistent_packed_batch_matches_one_cta(oracle_mod, one_lib):
     assert fa.fa_last_device_status() == fa.FA_OK
     ref = oracle_mod.attention_bwd_varlen(q, k, v, dO, cu, scale, causal)
     for name, a, b, r in zip(("dQ", "dK", "dV"), pers, one, ref):
-        check_grad(a, r, f"packed persistent {name}")
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"packed {name}: persistent and one-CTA differ"
+        check_grad(a, r, f"packed persistent d{d} causal={causal} {name}")
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+            f"packed d{d} causal={causal} {name}: persistent and one-CTA differ"
