@@ -63,6 +63,22 @@
 #ifndef FA_DKDV_PERSIST_MAX_N_CAUSAL
 #define FA_DKDV_PERSIST_MAX_N_CAUSAL 8192
 #endif
+// dQ (one CTA per query tile, head dims 64 and 128): persistent CTAs for
+// sequences up to these lengths.  Causal units range from 1 to N / 128 key
+// tiles; past 8192 rows at head dim 128 the strided static share of them
+// measured 1.5-2 % slower than the hardware's dynamic CTA scheduling.
+#ifndef FA_DQ_PERSIST_MAX_N
+#define FA_DQ_PERSIST_MAX_N (1 << 30)
+#endif
+#ifndef FA_DQ_PERSIST_MAX_N_CAUSAL
+#define FA_DQ_PERSIST_MAX_N_CAUSAL (1 << 30)
+#endif
+#ifndef FA_DQ128_PERSIST_MAX_N
+#define FA_DQ128_PERSIST_MAX_N (1 << 30)
+#endif
+#ifndef FA_DQ128_PERSIST_MAX_N_CAUSAL
+#define FA_DQ128_PERSIST_MAX_N_CAUSAL 8192
+#endif
 // The same at head dim 128, where the one-CTA kernel runs up to FA_DKDV_PAIR_MIN_N
 // (_CAUSAL) rows; at causal 4096 rows the two forms measured the same.
 #ifndef FA_DKDV128_PERSIST_MAX_N
@@ -1622,9 +1638,11 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__
 //   dS = P (dP - D)             -> TMEM over dP (bf16, dQ's A operand)
 // PAIR: the kernel runs as a CTA pair whose rank-0 CTA issues the MMAs; the S
 // and dS signals go to that CTA's barriers.
+// gj0: iterations the CTA ran before this work unit (barrier phases and dP
+// buffers count across units).
 template <class C, bool CAUSAL, bool PAIR = false>
 __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint32_t tmem, const WaitCtx &wctx,
-                                        int warp, int nb, int q_row, float lse2, float dlt, int L) {
+                                        int warp, int nb, int q_row, float lse2, float dlt, int L, int gj0 = 0) {
   auto bar = [&](int i) { return bar0 + 8u * i; };
   auto signal_mma = [&](int i) {  // the MMA-issuing CTA's barrier i
     if (PAIR) mbar_arrive_warp_cluster(mapa_shared(bar(i), 0));
@@ -1638,10 +1656,11 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
   const uint32_t dp_tm0 = tmem + lane_off + C::kColDP + KW * wg;  // dP columns of this warpgroup (buffer 0)
   bool ok = true;
   for (int j = 0; j < nb && ok; ++j) {
-    const int db = j % C::kDPBufs;  // dP buffer of this key tile
+    const unsigned gj = (unsigned)(gj0 + j);  // iteration count over the CTA's units
+    const unsigned db = gj % C::kDPBufs;      // dP buffer of this key tile
     const uint32_t dp_tm = dp_tm0 + 128u * db;
     const uint32_t ds_tm = dp_tm;  // dS (bf16) over the first KW / 2 of this warpgroup's dP columns
-    ok = mbar_wait_warp(bar(C::kBarS), j & 1, wctx, kBSiteS);
+    ok = mbar_wait_warp(bar(C::kBarS), gj & 1u, wctx, kBSiteS);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 0);
     tc_fence_after();
@@ -1669,7 +1688,7 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
       for (int c = 0; c < KW; ++c)
         if (c > lim) pe[c] = 0.f;
     }
-    ok = mbar_wait_warp(bar(C::kBarDP + db), (j / C::kDPBufs) & 1, wctx, kBSiteDP);
+    ok = mbar_wait_warp(bar(C::kBarDP + db), (gj / C::kDPBufs) & 1u, wctx, kBSiteDP);
     if (!ok) break;
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 1);
     tc_fence_after();
@@ -1693,14 +1712,14 @@ __device__ __forceinline__ bool dq_rows(const BwdParams &p, uint32_t bar0, uint3
       tmem_st_32x32b_x16(ds_tm, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
     tmem_wait_st();
     tc_fence_before();
-    if (!(FA_STALL(3) && j == 0)) signal_mma(C::kBarDS + db);
+    if (!(FA_STALL(3) && gj == 0)) signal_mma(C::kBarDS + db);
     if (threadIdx.x == 0) FA_TRACE_EV(1, j, 2);
   }
   return ok;
 }
 
 // ================================================================== dQ
-template <int D>
+template <int D, bool PERSIST = false>
 struct DqCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kStages = (D == 64) ? 14 : 7;  // ring slots of one tile
@@ -1709,15 +1728,20 @@ struct DqCfg {
   // so neither load waits on the other's late release.
   static constexpr int kKSlots = (4 * kStages + 6) / 7;  // 7 -> 4, 14 -> 8
   static constexpr int kVSlots = kStages - kKSlots;
-  // fill 0 = Q, 1 = dO, 2 + 2 j = K_j, 3 + 2 j = V_j
+  // a unit's fills: 0 = Q, 1 = dO, 2 + 2 j = K_j, 3 + 2 j = V_j (counted on over
+  // the CTA's units, from 0: unsigned arithmetic)
   __device__ static int slot(int fill) {
-    const int m = fill >> 1;
-    return (fill & 1) ? kKSlots + m % kVSlots : m % kKSlots;
+    const unsigned m = (unsigned)fill >> 1;
+    return (int)((fill & 1) ? kKSlots + m % kVSlots : m % kKSlots);
   }
   __device__ static uint32_t phase(int fill) {
-    const int m = fill >> 1;
-    return (uint32_t)(((fill & 1) ? m / kVSlots : m / kKSlots) & 1);
+    const unsigned m = (unsigned)fill >> 1;
+    return ((fill & 1) ? m / kVSlots : m / kKSlots) & 1u;
   }
+  // PERSIST: at most one CTA per SM, each running work units blockIdx.x,
+  // blockIdx.x + gridDim.x, ...; the epilogue then writes dQ rows straight to
+  // global memory (the ring already holds the next unit's tiles).
+  static constexpr bool kPersist = PERSIST;
   // Elementwise warpgroups: thread = query row, a warpgroup per 128 / kNumWG
   // key columns (four at head dim 64 measured 3-4 % slower than two, as for
   // the dK/dV kernel).
@@ -1742,9 +1766,40 @@ struct DqCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-  using C = DqCfg<D>;
+// One work unit of the one-CTA dQ kernel: query tile it_q of one (batch, head).
+struct DqUnit {
+  SeqSpan sq;
+  int b, h, kh, q0, nb;
+  bool skip;  // packed batch: the tile lies past its sequence, no rows to produce
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ DqUnit dq_unit(const BwdParams &p, int u) {
+  DqUnit w;
+  const int n_q = (p.N + 127) / 128;
+  int rank, head;
+  work_order(u, n_q, p.B * p.H, p.sched_chunk, rank, head);
+  const int it_q = CAUSAL ? n_q - 1 - rank : rank;  // causal: the longest query rows first
+  w.h = head % p.H;
+  w.b = head / p.H;
+  w.kh = w.h / (p.H / p.Hkv);
+  w.q0 = it_q * 128;
+  w.sq = VARLEN ? seq_span(p.cu_seqlens, w.b, p.N, p.total) : SeqSpan{0, p.N, w.b};
+  w.skip = VARLEN && w.q0 >= w.sq.len;
+  w.nb = CAUSAL ? it_q + 1 : (w.sq.len + 127) / 128;  // key tiles this query tile sees
+  return w;
+}
+
+// The CTA runs work units blockIdx.x, blockIdx.x + gridDim.x, ... (PERSIST: at
+// most one CTA per SM; else one unit per CTA).  A unit's ring fills are Q, dO,
+// then K_j, V_j for its key tiles: the producer issues the next unit's Q and
+// dO right after this unit's last K and V.  The elementwise warps copy them
+// into TMEM after this unit's epilogue has waited for its last MMA, so the S
+// and dP MMAs that read the previous Q and dO are done.  Every ring, dP buffer
+// and barrier phase counts over the CTA's units.
+template <int D, bool CAUSAL, bool VARLEN, bool PERSIST>
+__global__ void __launch_bounds__(DqCfg<D, PERSIST>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = DqCfg<D, PERSIST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (!check_align(sbase, p.status)) return;
@@ -1759,17 +1814,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_q = (p.N + 127) / 128;
-  int rank, head;
-  work_order((int)blockIdx.x, n_q, p.B * p.H, p.sched_chunk, rank, head);
-  const int it_q = CAUSAL ? n_q - 1 - rank : rank;  // causal: the longest query rows first
-  const int h = head % p.H, b = head / p.H;
-  const int kh = h / (p.H / p.Hkv);
   const int Npad = n_q * 128;  // row-term arrays are [B, H, Npad]
-  const int q0 = it_q * 128;
-  const SeqSpan sq = VARLEN ? seq_span(p.cu_seqlens, b, p.N, p.total) : SeqSpan{0, p.N, b};
-  const int L = sq.len;  // rows of this sequence
-  if (VARLEN && q0 >= L) return;  // the tile lies past its sequence: no rows to produce
-  const int nb = CAUSAL ? it_q + 1 : (L + 127) / 128;  // key tiles this query tile sees
+  const int n_units = n_q * p.B * p.H;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumBars; ++i)
@@ -1799,63 +1845,80 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
 
   if (warp < 4 * C::kNumWG) {
     // ===================================================== dS = P (dP - D), one warpgroup per 128 / kNumWG key columns
+    // After a wait has run out the loop ends (the named barrier of the staged
+    // epilogue belongs to the one-unit form, which runs the loop once).
     const int wg = warp >> 2;
     const int r = threadIdx.x & 127;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int q_row = q0 + r;
-    if (wg < 2) {
-      // Q (warpgroup 0) or dO (warpgroup 1): ring fill 0 / 1 (TMA, zero rows
-      // past N); this thread's row, bf16 pairs in memory order, into TMEM as the
-      // A operand of the S / dP MMAs.
-      uint32_t row[D / 2];
-      const bool got = mbar_wait_warp(bar(C::kBarFull0 + C::slot(wg)), 0, wctx, kBSiteQ);
-      const uint8_t *tile = smem + C::kOffRing + C::slot(wg) * C::kTile;
+    bool ok = true;
+    int gj = 0, uc = 0;  // iterations and units this CTA has run
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const DqUnit w = dq_unit<CAUSAL, VARLEN>(p, u);
+      if (w.skip) continue;
+      const int q_row = w.q0 + r;
+      if (wg < 2) {
+        // Q (warpgroup 0) or dO (warpgroup 1): this unit's ring fill 0 / 1
+        // (TMA, zero rows past N); this thread's row, bf16 pairs in memory
+        // order, into TMEM as the A operand of the S / dP MMAs.
+        const int fill = 2 * uc + 2 * gj + wg;
+        uint32_t row[D / 2];
+        const bool got = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fill)), C::phase(fill), wctx, kBSiteQ);
+        const uint8_t *tile = smem + C::kOffRing + C::slot(fill) * C::kTile;
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v) {
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (got) x = *reinterpret_cast<const uint4 *>(tile + (v >> 3) * 16384 + r * 128 + (((v & 7) ^ (r & 7)) << 4));
-        row[4 * v] = x.x;
-        row[4 * v + 1] = x.y;
-        row[4 * v + 2] = x.z;
-        row[4 * v + 3] = x.w;
-      }
-      const uint32_t dst = tmem + lane_off + (wg == 0 ? C::kColQ : C::kColDO);
+        for (int v = 0; v < D / 8; ++v) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (got) x = *reinterpret_cast<const uint4 *>(tile + (v >> 3) * 16384 + r * 128 + (((v & 7) ^ (r & 7)) << 4));
+          row[4 * v] = x.x;
+          row[4 * v + 1] = x.y;
+          row[4 * v + 2] = x.z;
+          row[4 * v + 3] = x.w;
+        }
+        const uint32_t dst = tmem + lane_off + (wg == 0 ? C::kColQ : C::kColDO);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&row[32 * c]);
-        tmem_st_32x32b_x32(dst + 32 * c, part);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&row[32 * c]);
+          tmem_st_32x32b_x32(dst + 32 * c, part);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive_warp(bar(C::kBarQdo));
+        if (threadIdx.x == 0) FA_LIFE(1, 2);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive_warp(bar(C::kBarQdo));
-      if (threadIdx.x == 0) FA_LIFE(1, 2);
-    }
-    const size_t rw = ((size_t)b * p.H + h) * Npad + q_row;
-    const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
-    const float dlt = p.delta[rw];
-    bool ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, nb, q_row, lse2, dlt, L);
-    // ---- epilogue (warpgroups 0 and 1, half the head dim each): dQ * scale -> bf16 -> shared staging -> TMA store
-    if (wg < 2) {
-    if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), 0, wctx, kBSiteFinal);
-    if (threadIdx.x == 0) FA_LIFE(1, 4);
-    tc_fence_after();
-    uint8_t *stage = smem + C::kOffStage;
-    const bool direct = VARLEN && q0 + 128 > L;  // the next sequence's rows follow: write row by row
-    if (ok && direct)
-      acc_to_global<D / 2>(tmem + lane_off + C::kColDQ,
-                           static_cast<__nv_bfloat16 *>(p.dq) + ((size_t)(sq.start + q_row) * p.H + h) * D, wg * (D / 2),
-                           p.scale, q_row < L);
-    else if (ok)
-      acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
-    fence_proxy_async_smem();
-    named_bar_sync(1, 256);
-    if (threadIdx.x == 0 && ok && !direct) {
-      for (int bx = 0; bx < D / 64; ++bx)
-        tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, h, sq.start + q0, sq.bc);
-      bulk_commit();
-      bulk_wait_read_all();
-      if (threadIdx.x == 0) FA_LIFE(1, 5);
-    }
+      const size_t rw = ((size_t)w.b * p.H + w.h) * Npad + q_row;
+      const float lse2 = p.lse2[rw];  // +inf on padded rows: P = 0
+      const float dlt = p.delta[rw];
+      if (ok) ok = dq_rows<C, CAUSAL>(p, bar0, tmem, wctx, warp, w.nb, q_row, lse2, dlt, w.sq.len, gj);
+      gj += w.nb;
+      // ---- epilogue (warpgroups 0 and 1, half the head dim each): dQ * scale -> bf16 -> global memory
+      if (wg < 2) {
+        if (ok) ok = mbar_wait_warp(bar(C::kBarFinal), uc & 1, wctx, kBSiteFinal);
+        if (threadIdx.x == 0) FA_LIFE(1, 4);
+        tc_fence_after();
+        // straight from TMEM, a query row per thread: persistent CTAs (the ring
+        // already holds the next unit's tiles), or the next sequence's rows follow
+        const bool direct = C::kPersist || (VARLEN && w.q0 + 128 > w.sq.len);
+        const size_t row0 = VARLEN ? (size_t)w.sq.start : (size_t)w.b * p.N;  // the sequence's first row
+        if (ok && direct)
+          acc_to_global<D / 2>(tmem + lane_off + C::kColDQ,
+                               static_cast<__nv_bfloat16 *>(p.dq) + ((row0 + q_row) * p.H + w.h) * D, wg * (D / 2),
+                               p.scale, q_row < w.sq.len);
+        tc_fence_before();  // the accumulator reads precede the next unit's first dQ MMA
+        if (!C::kPersist) {
+          uint8_t *stage = smem + C::kOffStage;
+          if (ok && !direct) acc_to_smem<D / 2>(tmem + lane_off + C::kColDQ, stage, r, wg * (D / 2), p.scale);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 256);
+          if (threadIdx.x == 0 && ok && !direct) {
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_store_4d(&p.tm_dq, sbase + C::kOffStage + bx * 16384, bx * 64, w.h, w.sq.start + w.q0, w.sq.bc);
+            bulk_commit();
+            bulk_wait_read_all();
+            if (threadIdx.x == 0) FA_LIFE(1, 5);
+          }
+        }
+      }
+      ++uc;
+      if (!C::kPersist) break;  // one unit per CTA
     }
   } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issue
@@ -1864,8 +1927,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
     // dS_j (bf16, over the dP columns) is read by dQ_j, which precedes dP_{j+1}
     // (the tensor pipe runs one thread's MMAs in order).  With two dP buffers
     // the order is S_{j+1} dP_{j+1} [dS_j] dQ_j: dP_{j+1} goes to the buffer of
-    // dS_{j-1}, whose dQ_{j-1} was issued before it.  The whole warp runs the
-    // loop and waits; the elected lane issues.
+    // dS_{j-1}, whose dQ_{j-1} was issued before it.  Iterations count over
+    // the CTA's units; a unit's first S and dP follow its Q and dO in TMEM,
+    // copied after the previous unit's epilogue read its dQ.  The whole warp
+    // runs the loop and waits; the elected lane issues.
     {
       constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);  // S, dP (A in TMEM, B K-major)
       constexpr uint32_t id_dq = make_idesc_bf16(128, D, false, true);    // dQ (A = dS in TMEM, B = K MN-major)
@@ -1877,92 +1942,103 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
       // dS of warpgroup w (its KW key columns, bf16 pairs) starts at column KW w
       constexpr int KW = 128 / C::kNumWG, KPW = KW / 16;
       auto a_col = [](int kk) { return (uint32_t)(KW * (kk / KPW) + 8 * (kk % KPW)); };
-      // ring fills 0 and 1 held Q and dO; K_j is fill 2 + 2j, V_j fill 3 + 2j
-      auto fk = [](int j) { return 2 + 2 * j; };
-      auto fv = [](int j) { return 3 + 2 * j; };
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T
+      auto issue_s = [&](int fk_) {  // S = Q K^T   (K from ring fill fk_)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(fk(j)) + kmaj(kk), id_s, kk > 0);
+            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8u * kk, ring_d + slot_off(fk_) + kmaj(kk), id_s, kk > 0);
           tc_commit(bar(C::kBarS));
         }
         __syncwarp();
       };
-      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T, into buffer j % kDPBufs
-        const int db = j % C::kDPBufs;
+      auto issue_dp = [&](unsigned gjj, int fv_) {  // dP = dO V^T into buffer gjj % kDPBufs   (V from fill fv_)
+        const unsigned db = gjj % C::kDPBufs;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColDP + 128u * db, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv(j)) + kmaj(kk),
+            mma_ts(tmem + C::kColDP + 128u * db, tmem + C::kColDO + 8u * kk, ring_d + slot_off(fv_) + kmaj(kk),
                    id_s, kk > 0);
           tc_commit(bar(C::kBarDP + db));
-          tc_commit(bar(C::kBarEmpty0 + C::slot(fv(j))));  // V_j consumed
+          tc_commit(bar(C::kBarEmpty0 + C::slot(fv_)));  // V consumed
         }
         __syncwarp();
       };
-      bool ok = mbar_wait_warp(bar(C::kBarQdo), 0, wctx, kBSiteQ);
-      // Q and dO are in TMEM: their slots (the first of the K ring and of the V ring) may take K/V fills
-      if (ok && elect_one()) {
-        mbar_arrive(bar(C::kBarEmpty0 + C::slot(0)));
-        mbar_arrive(bar(C::kBarEmpty0 + C::slot(1)));
-      }
-      __syncwarp();
-      if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(0))), par(fk(0)), wctx, kBSiteFull);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        if (lane == 0) FA_LIFE(1, 3);
-        ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(0))), par(fv(0)), wctx, kBSiteFull);
-      }
-      if (ok) {
-        tc_fence_after();
-        issue_dp(0);
-      }
-      for (int j = 0; j < nb && ok; ++j) {
-        FA_TRACE_EV(1, j, 8);
-        const bool more = j + 1 < nb;
-        if (more) {
-          ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, wctx, kBSiteS);
-          FA_TRACE_EV(1, j, 12);
-          if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(j + 1))), par(fk(j + 1)), wctx, kBSiteFull);
-          if (!ok) break;
-          FA_TRACE_EV(1, j, 13);
+      bool ok = true;
+      int gj = 0, uc = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL, VARLEN>(p, u);
+        if (w.skip) continue;
+        const int nb = w.nb;
+        const int fb = 2 * uc + 2 * gj;  // this unit's first ring fill (Q; dO at fb + 1)
+        // K_j is fill fb + 2 + 2 j, V_j fill fb + 3 + 2 j
+        auto fk = [&](int j) { return fb + 2 + 2 * j; };
+        auto fv = [&](int j) { return fb + 3 + 2 * j; };
+        ok = mbar_wait_warp(bar(C::kBarQdo), uc & 1, wctx, kBSiteQ);
+        // Q and dO are in TMEM: their ring slots may take later fills
+        if (ok && elect_one()) {
+          mbar_arrive(bar(C::kBarEmpty0 + C::slot(fb)));
+          mbar_arrive(bar(C::kBarEmpty0 + C::slot(fb + 1)));
+        }
+        __syncwarp();
+        if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(0))), par(fk(0)), wctx, kBSiteFull);
+        if (ok) {
           tc_fence_after();
-          issue_s(j + 1);
-          if (C::kDPBufs == 2) {
+          issue_s(fk(0));
+          if (uc == 0 && lane == 0) FA_LIFE(1, 3);
+          ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(0))), par(fv(0)), wctx, kBSiteFull);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_dp((unsigned)gj, fv(0));
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+          const unsigned gjj = (unsigned)(gj + j);
+          FA_TRACE_EV(1, j, 8);
+          const bool more = j + 1 < nb;
+          if (more) {
+            ok = mbar_wait_warp(bar(C::kBarSFree), gjj & 1u, wctx, kBSiteS);
+            FA_TRACE_EV(1, j, 12);
+            if (ok) ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fk(j + 1))), par(fk(j + 1)), wctx, kBSiteFull);
+            if (!ok) break;
+            FA_TRACE_EV(1, j, 13);
+            tc_fence_after();
+            issue_s(fk(j + 1));
+            if (C::kDPBufs == 2) {
+              ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
+              if (!ok) break;
+              tc_fence_after();
+              issue_dp(gjj + 1, fv(j + 1));
+            }
+          }
+          const unsigned db = gjj % C::kDPBufs;
+          ok = mbar_wait_warp(bar(C::kBarDS + db), (gjj / C::kDPBufs) & 1u, wctx, kBSiteDS);
+          if (!ok) break;
+          FA_TRACE_EV(1, j, 9);
+          tc_fence_after();
+          // dQ += dS_j K_j
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + C::kColDQ, tmem + C::kColDP + 128u * db + a_col(kk),
+                     ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
+            tc_commit(bar(C::kBarEmpty0 + C::slot(fk(j))));  // K_j consumed
+          }
+          __syncwarp();
+          if (C::kDPBufs == 1 && more) {
             ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
             if (!ok) break;
             tc_fence_after();
-            issue_dp(j + 1);
+            issue_dp(gjj + 1, fv(j + 1));
           }
+          FA_TRACE_EV(1, j, 10);
         }
-        const int db = j % C::kDPBufs;
-        ok = mbar_wait_warp(bar(C::kBarDS + db), (j / C::kDPBufs) & 1, wctx, kBSiteDS);
-        if (!ok) break;
-        FA_TRACE_EV(1, j, 9);
-        tc_fence_after();
-        // dQ += dS_j K_j
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::kColDQ, tmem + C::kColDP + 128u * db + a_col(kk),
-                   ring_mn + slot_off(fk(j)) + (uint64_t)(kk * 128), id_dq, (j > 0 || kk > 0));
-          tc_commit(bar(C::kBarEmpty0 + C::slot(fk(j))));  // K_j consumed
-        }
+        if (elect_one()) tc_commit(bar(C::kBarFinal));  // the unit's dQ is complete
         __syncwarp();
-        if (C::kDPBufs == 1 && more) {
-          ok = mbar_wait_warp(bar(C::kBarFull0 + C::slot(fv(j + 1))), par(fv(j + 1)), wctx, kBSiteFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp(j + 1);
-        }
-        FA_TRACE_EV(1, j, 10);
+        gj += nb;
+        ++uc;
+        if (!C::kPersist) break;
       }
-      if (elect_one()) {
-        tc_commit(bar(C::kBarFinal));
-        tc_commit(bar(C::kBarDrain));
-      }
+      if (elect_one()) tc_commit(bar(C::kBarDrain));
       __syncwarp();
       if (!mbar_wait_warp(bar(C::kBarDrain), 0, wctx, kBSiteDrain) && *abort_flag) {
         const uint64_t t0 = global_timer_ns();
@@ -1970,32 +2046,36 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1) bwd_dq_kernel(const __g
       }
     }
   } else {
-    // ===================================================== TMA producer: Q, dO, then K_j and V_j in turn, each into its own ring
+    // ===================================================== TMA producer: per unit Q, dO, then K_j and V_j in turn, each into its own ring
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();  // K, V are re-read by every query tile
       const uint64_t once = policy_evict_first();  // this CTA's Q and dO rows are read once
-      // fills 0, 1: Q and dO (fresh slots; the MMA warp releases them once the
-      // elementwise warps have copied them into TMEM)
-      for (int t = 0; t < 2; ++t) {
-        const int st = C::slot(t);
-        mbar_arrive_expect_tx(bar(C::kBarFull0 + st), C::kTile);
-        for (int bx = 0; bx < D / 64; ++bx)
-          tma_load_4d_hint(sbase + C::kOffRing + st * C::kTile + bx * 16384, t ? &p.tm_do : &p.tm_q,
-                           bar(C::kBarFull0 + st), bx * 64, h, sq.start + q0, sq.bc, once);
-      }
       bool ok = true;
-      int fill = 2;
-      for (int j = 0; j < nb && ok; ++j) {
-        for (int kv = 0; kv < 2 && ok; ++kv, ++fill) {
+      int fill = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DqUnit w = dq_unit<CAUSAL, VARLEN>(p, u);
+        if (w.skip) continue;
+        // Q and dO of this unit (the MMA warp releases their slots once the
+        // elementwise warps have copied them into TMEM), then K_j, V_j
+        for (int t = 0; t < 2 + 2 * w.nb && ok; ++t, ++fill) {
           const int s = C::slot(fill);
           ok = mbar_wait(bar(C::kBarEmpty0 + s), C::phase(fill) ^ 1, wctx, kBSiteEmpty);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(C::kBarFull0 + s), C::kTile);
-          const CUtensorMap *map = kv ? &p.tm_v : &p.tm_k;
-          for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_4d_hint(sbase + C::kOffRing + s * C::kTile + bx * 16384, map, bar(C::kBarFull0 + s), bx * 64, kh,
-                             sq.start + j * 128, sq.bc, keep);
+          const uint32_t dst = sbase + C::kOffRing + s * C::kTile;
+          if (t < 2) {
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_load_4d_hint(dst + bx * 16384, t ? &p.tm_do : &p.tm_q, bar(C::kBarFull0 + s), bx * 64, w.h,
+                               w.sq.start + w.q0, w.sq.bc, once);
+          } else {
+            const int j = (t - 2) >> 1;
+            const CUtensorMap *map = (t & 1) ? &p.tm_v : &p.tm_k;
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_load_4d_hint(dst + bx * 16384, map, bar(C::kBarFull0 + s), bx * 64, w.kh, w.sq.start + j * 128,
+                               w.sq.bc, keep);
+          }
         }
+        if (!C::kPersist) break;
       }
       const uint64_t t0 = global_timer_ns();
       // the last issued fill of each slot: the last kKSlots even fills, the last kVSlots odd ones
@@ -3706,13 +3786,24 @@ int launch_dq_pair_t(const BwdParams &p_in, cudaStream_t stream) {
 template <int D, bool CAUSAL>
 int launch_dq_t(const BwdParams &p_in, cudaStream_t stream) {
   const BwdParams p = with_q_order(p_in, CAUSAL, D);
-  const unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
+  unsigned grid = grid_1d((p.N + 127) / 128, (long long)p.B * p.H);
   if (!grid) return FA_ERR_UNSUPPORTED;
+  const int max_n = CAUSAL ? (D == 64 ? FA_DQ_PERSIST_MAX_N_CAUSAL : FA_DQ128_PERSIST_MAX_N_CAUSAL)
+                           : (D == 64 ? FA_DQ_PERSIST_MAX_N : FA_DQ128_PERSIST_MAX_N);
+  if (p.N <= max_n) {  // persistent CTAs: at most one per SM
+    using PC = DqCfg<D, true>;
+    const int sms = sm_count();
+    if (sms > 0 && grid > (unsigned)sms) grid = (unsigned)sms;
+    return p.cu_seqlens
+               ? launch_kernel(bwd_dq_kernel<D, CAUSAL, true, true>, dim3(grid), PC::kThreads, PC::kSmemBytes, p, stream)
+               : launch_kernel(bwd_dq_kernel<D, CAUSAL, false, true>, dim3(grid), PC::kThreads, PC::kSmemBytes, p,
+                               stream);
+  }
   return p.cu_seqlens
-             ? launch_kernel(bwd_dq_kernel<D, CAUSAL, true>, dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, p,
-                             stream)
-             : launch_kernel(bwd_dq_kernel<D, CAUSAL, false>, dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes, p,
-                             stream);
+             ? launch_kernel(bwd_dq_kernel<D, CAUSAL, true, false>, dim3(grid), DqCfg<D>::kThreads, DqCfg<D>::kSmemBytes,
+                             p, stream)
+             : launch_kernel(bwd_dq_kernel<D, CAUSAL, false, false>, dim3(grid), DqCfg<D>::kThreads,
+                             DqCfg<D>::kSmemBytes, p, stream);
 }
 
 }  // namespace

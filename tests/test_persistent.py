@@ -1,14 +1,15 @@
-"""Persistent dK/dV CTAs against one CTA per key tile, at head dims 64 and 128.
+"""Persistent dK/dV and dQ CTAs against one CTA per tile, at head dims 64 and 128.
 
 The default library runs the one-CTA dK/dV kernel (head dim 64, and 128 up to
-the lengths where the CTA pairs take over) on at most one CTA per SM, each
-taking key-tile units blockIdx.x, blockIdx.x + gridDim.x, ... and carrying its
-rings, TMEM buffers and barrier phases from one unit into the next (the next
-unit's K and V load as soon as the last MMA that read the previous ones
-completes); at head dim 128 its epilogue writes each key row straight to
-global memory.  Causal head-dim-64 sequences longer than 8192 rows run one CTA
-per unit instead.  A build with every threshold at 0 runs every shape one CTA
-per unit.  Both must match the oracle, and they must give bitwise equal
+the lengths where the CTA pairs take over) and the dQ kernel on at most one CTA
+per SM, each taking tile units blockIdx.x, blockIdx.x + gridDim.x, ... and
+carrying its rings, TMEM buffers and barrier phases from one unit into the
+next (dK/dV: the next unit's K and V load as soon as the last MMA that read
+the previous ones completes; dQ: the next unit's Q and dO follow this unit's
+last K and V in the ring).  Epilogues without a stage of their own write each
+row straight to global memory.  Some long causal shapes run one CTA per unit
+instead.  A build with every threshold at 0 runs every shape one CTA per
+unit.  Both must match the oracle, and they must give bitwise equal
 gradients: each unit's MMAs see the same bf16 operands in the same order
 whichever CTA runs it.  The shapes give block 0 several units (more units than
 SMs), with GQA, ragged tails, the causal mask and a packed batch whose short
@@ -30,9 +31,11 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 @pytest.fixture(scope="module")
 def one_lib(tmp_path_factory):
-    path = str(tmp_path_factory.mktemp("onecta") / "libfa_dkdv1.so")
+    path = str(tmp_path_factory.mktemp("onecta") / "libfa_onecta.so")
     build.build(force=True, extra_flags=["-DFA_DKDV_PERSIST_MAX_N=0", "-DFA_DKDV_PERSIST_MAX_N_CAUSAL=0",
-                                         "-DFA_DKDV128_PERSIST_MAX_N=0", "-DFA_DKDV128_PERSIST_MAX_N_CAUSAL=0"],
+                                         "-DFA_DKDV128_PERSIST_MAX_N=0", "-DFA_DKDV128_PERSIST_MAX_N_CAUSAL=0",
+                                         "-DFA_DQ_PERSIST_MAX_N=0", "-DFA_DQ_PERSIST_MAX_N_CAUSAL=0",
+                                         "-DFA_DQ128_PERSIST_MAX_N=0", "-DFA_DQ128_PERSIST_MAX_N_CAUSAL=0"],
                 lib_path=path)
     lib = ctypes.CDLL(path)
     for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_last_device_status"):
@@ -43,7 +46,7 @@ def one_lib(tmp_path_factory):
 
 
 CASES = [
-    # B, N, H, Hkv, causal: (N / 128 rounded up) * B * Hkv key-tile units
+    # B, N, H, Hkv, causal: (N / 128 rounded up) * B * Hkv key-tile units, * B * H query-tile units
     (8, 333, 8, 8, False),   # 192 units, ragged last tile
     (8, 333, 16, 8, True),   # 192 units, GQA groups of two, causal
     (16, 640, 4, 2, True),   # 160 units of 1-5 query tiles each
@@ -53,7 +56,7 @@ CASES = [
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,N,H,Hkv,causal", CASES)
-def test_persistent_and_one_cta_dkdv_agree_and_match_oracle(oracle_mod, one_lib, B, N, H, Hkv, causal, d):
+def test_persistent_and_one_cta_agree_and_match_oracle(oracle_mod, one_lib, B, N, H, Hkv, causal, d):
     seed = 7300 + N + H + causal + d
     q = inputs.random_bf16((B, N, H, d), seed, "cuda")
     k = inputs.random_bf16((B, N, Hkv, d), seed + 1, "cuda")

@@ -67,12 +67,13 @@ def test_default_build_has_no_stall_hook():
     assert fa.lib().fa_debug_stall(1) == fa.FA_ERR_UNSUPPORTED
 
 
-# (mode, causal, B, H, d).  The one-CTA dK/dV kernel is persistent: with 320
-# work units on at most one CTA per SM, block 0 runs several, and after the
-# stall in its first unit it must step through the rest and still return
-# (causal head-dim-128 shapes take the CTA pairs in this build).
+# (mode, causal, B, H, d).  The one-CTA dK/dV kernel and the dQ kernel are
+# persistent: with 320 work units on at most one CTA per SM, block 0 runs
+# several, and after the stall in its first unit it must still return (causal
+# head-dim-128 dK/dV takes the CTA pairs in this build).
 CASES = [(1, True, 1, 2, 128), (2, True, 1, 2, 128), (2, False, 1, 2, 128), (3, True, 1, 2, 128),
-         (2, True, 4, 16, 64), (2, False, 4, 16, 64), (2, False, 4, 16, 128)]
+         (2, True, 4, 16, 64), (2, False, 4, 16, 64), (2, False, 4, 16, 128), (3, False, 4, 16, 64),
+         (3, True, 4, 16, 128)]
 
 
 @pytest.mark.parametrize("mode,causal,B,H,d", CASES)
