@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -41,6 +42,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: 
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = nvcc_path()
     tag = "x".join(f for f in extra_flags).replace("-", "").replace("=", "") or "default"
+    if len(tag) > 64:  # keep object names within the file system's limit
+        tag = "v" + hashlib.sha256(tag.encode()).hexdigest()[:16]
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + f".{tag}.o")

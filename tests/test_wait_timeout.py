@@ -73,7 +73,7 @@ def test_default_build_has_no_stall_hook():
 # head-dim-128 dK/dV takes the CTA pairs in this build).
 CASES = [(1, True, 1, 2, 128), (2, True, 1, 2, 128), (2, False, 1, 2, 128), (3, True, 1, 2, 128),
          (2, True, 4, 16, 64), (2, False, 4, 16, 64), (2, False, 4, 16, 128), (3, False, 4, 16, 64),
-         (3, True, 4, 16, 128)]
+         (3, True, 4, 16, 128), (1, True, 4, 16, 128)]
 
 
 @pytest.mark.parametrize("mode,causal,B,H,d", CASES)
