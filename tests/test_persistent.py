@@ -1,12 +1,14 @@
-"""Persistent dK/dV and dQ CTAs against one CTA per tile, at head dims 64 and 128.
+"""Persistent CTAs against one CTA (or CTA pair) per tile.
 
 The default library runs the one-CTA dK/dV kernel (head dim 64, and 128 up to
-the lengths where the CTA pairs take over) and the dQ kernel on at most one CTA
-per SM, each taking tile units blockIdx.x, blockIdx.x + gridDim.x, ... and
+the lengths where the CTA pairs take over), the dQ kernel (head dims 64 and
+128) and the head-dim-256 CTA-pair forward on at most one CTA (pair) per SM
+(pair), each taking tile units blockIdx.x, blockIdx.x + gridDim.x, ... and
 carrying its rings, TMEM buffers and barrier phases from one unit into the
 next (dK/dV: the next unit's K and V load as soon as the last MMA that read
 the previous ones completes; dQ: the next unit's Q and dO follow this unit's
-last K and V in the ring).  Epilogues without a stage of their own write each
+last K and V in the ring; pair forward: each CTA loads its next Q tile once the
+unit's last S has read the previous one).  Epilogues without a stage of their own write each
 row straight to global memory.  Some long causal shapes run one CTA per unit
 instead.  A build with every threshold at 0 runs every shape one CTA per
 unit.  Both must match the oracle, and they must give bitwise equal
@@ -24,7 +26,7 @@ import torch
 
 import exact_attention_blackwell_gb300 as fa
 from exact_attention_blackwell_gb300 import build, inputs
-from helpers import check_grad
+from helpers import check_grad, check_lse, check_o
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -35,10 +37,12 @@ def one_lib(tmp_path_factory):
     build.build(force=True, extra_flags=["-DFA_DKDV_PERSIST_MAX_N=0", "-DFA_DKDV_PERSIST_MAX_N_CAUSAL=0",
                                          "-DFA_DKDV128_PERSIST_MAX_N=0", "-DFA_DKDV128_PERSIST_MAX_N_CAUSAL=0",
                                          "-DFA_DQ_PERSIST_MAX_N=0", "-DFA_DQ_PERSIST_MAX_N_CAUSAL=0",
-                                         "-DFA_DQ128_PERSIST_MAX_N=0", "-DFA_DQ128_PERSIST_MAX_N_CAUSAL=0"],
+                                         "-DFA_DQ128_PERSIST_MAX_N=0", "-DFA_DQ128_PERSIST_MAX_N_CAUSAL=0",
+                                         "-DFA_FWD_PAIR_PERSIST_MAX_N=0", "-DFA_FWD_PAIR_PERSIST_MAX_N_CAUSAL=0"],
                 lib_path=path)
     lib = ctypes.CDLL(path)
-    for name in ("fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen", "fa_last_device_status"):
+    for name in ("fa_fwd", "fa_fwd_varlen", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_varlen",
+                 "fa_last_device_status"):
         res, args = fa.SIGNATURES[name]
         getattr(lib, name).restype = res
         getattr(lib, name).argtypes = args
@@ -111,3 +115,58 @@ def test_persistent_packed_batch_matches_one_cta(oracle_mod, one_lib, d, causal)
         check_grad(a, r, f"packed persistent d{d} causal={causal} {name}")
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
             f"packed d{d} causal={causal} {name}: persistent and one-CTA differ"
+
+
+PAIR_FWD_CASES = [
+    # B, N, H, Hkv, causal: (N / 256 rounded up) * B * H units on at most 76 clusters
+    (4, 640, 8, 4, False),  # 96 units; the last pair's second tile half empty
+    (4, 640, 8, 4, True),
+    (1, 1, 1, 1, True),
+]
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,causal", PAIR_FWD_CASES)
+def test_persistent_pair_forward_matches_one_cluster_per_unit(oracle_mod, one_lib, B, N, H, Hkv, causal):
+    d = 256
+    seed = 7700 + N + H + causal
+    q = inputs.random_bf16((B, N, H, d), seed, "cuda")
+    k = inputs.random_bf16((B, N, Hkv, d), seed + 1, "cuda")
+    v = inputs.random_bf16((B, N, Hkv, d), seed + 2, "cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_fwd(q, k, v, scale=scale, causal=causal)
+    o1, lse1 = torch.empty_like(o), torch.empty_like(lse)
+    assert one_lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), lse1.data_ptr(), B, H, Hkv, N, d,
+                          scale, int(causal), None) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert one_lib.fa_last_device_status(None) == fa.FA_OK
+    assert fa.fa_last_device_status() == fa.FA_OK
+    what = f"d256 B{B} N{N} H{H}/{Hkv} causal={causal}"
+    assert torch.equal(o.view(torch.int16), o1.view(torch.int16)), f"{what}: O differs"
+    assert torch.equal(lse, lse1), f"{what}: LSE differs"
+    o_ref, lse_ref = oracle_mod.attention_fwd(q.cpu(), k.cpu(), v.cpu(), scale, causal)
+    check_o(o, o_ref, what)
+    check_lse(lse, lse_ref, what)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_pair_forward_packed_batch(oracle_mod, one_lib, causal):
+    lens = [(37 * i * i + 11 * i) % 700 for i in range(40)]  # 0-698 rows: 240 units, many past their sequence
+    H, Hkv, d = 2, 1, 256
+    total = sum(lens)
+    q = inputs.random_bf16((total, H, d), 7800, "cuda")
+    k = inputs.random_bf16((total, Hkv, d), 7801, "cuda")
+    v = inputs.random_bf16((total, Hkv, d), 7802, "cuda")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_fwd_varlen(q, k, v, cu, max(lens), scale=scale, causal=causal)
+    o1, lse1 = torch.empty_like(o), torch.empty_like(lse)
+    assert one_lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o1.data_ptr(), lse1.data_ptr(),
+                                 cu.data_ptr(), len(lens), max(lens), total, H, Hkv, d, scale, int(causal),
+                                 None) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert one_lib.fa_last_device_status(None) == fa.FA_OK
+    assert torch.equal(o.view(torch.int16), o1.view(torch.int16)), "packed d256: O differs"
+    assert torch.equal(lse, lse1), "packed d256: LSE differs"
+    o_ref, lse_ref = oracle_mod.attention_fwd_varlen(q, k, v, cu, scale, causal)
+    check_o(o, o_ref, f"packed d256 causal={causal}")
+    check_lse(lse, lse_ref, f"packed d256 causal={causal}")
