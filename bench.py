@@ -852,32 +852,76 @@ def run_varlen(args):
                         "flops_per_launch": 3.5 * fwd_f, "launch_ms": bwd_ms, "traffic": None},
            "gpu_launches": 4 * args.steps, "clocks": clocks}
     if not args.no_e2e:
-        pin = {n: x_cpu[n].pin_memory() for n in ("q", "k", "v", "dO")}
-        dsts = {"q": q, "k": k, "v": v, "dO": dO}
-        outs = [o, lse, dq, dk, dv]
-        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        # The same schedule as the fixed-length workloads: step i's uploads (s_in)
+        # overlap step i-1's kernels (s_cmp) and step i-2's downloads (s_out) over
+        # two device buffer sets; the kernels of all steps run in order on s_cmp,
+        # so they share one workspace.
+        names = ("q", "k", "v", "dO")
+        pin = {n: x_cpu[n].pin_memory() for n in names}
+        first_in = {"q": q, "k": k, "v": v, "dO": dO}
+        first_out = [o, lse, dq, dk, dv]
+        sets = [(first_in, first_out),
+                ({n: torch.empty_like(first_in[n]) for n in names}, [torch.empty_like(t) for t in first_out])]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in first_out]
+        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def e2e_step():
-            for n, h in pin.items():
-                dsts[n].copy_(h, non_blocking=True)
-            step()
-            for hd, dd in zip(outs_h, outs):
-                hd.copy_(dd, non_blocking=True)
+        def kernels(ins, outs, sp):
+            st = fa.fa_fwd_varlen(ins["q"], ins["k"], ins["v"], outs[0], outs[1], cu, B, L, T, H, Hkv, d, w.sm_scale,
+                                  w.causal, sp)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_fwd_varlen")
+            st = fa.fa_bwd_varlen(ins["q"], ins["k"], ins["v"], outs[0], outs[1], ins["dO"], outs[2], outs[3],
+                                  outs[4], cu, B, L, T, H, Hkv, d, w.sm_scale, w.causal, ws, nb, sp)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_bwd_varlen")
+
+        def pipeline(n_steps, e_start=None, e_end=None):
+            in_done, cmp_done, out_done = [], [], []
+            if e_start is not None:
+                e_start.record(s_in)
+            for i in range(n_steps):
+                ins, outs = sets[i % 2]
+                if i >= 2:
+                    s_in.wait_event(cmp_done[i - 2])  # step i-2 has finished reading this input set
+                with torch.cuda.stream(s_in):
+                    for n in names:
+                        ins[n].copy_(pin[n], non_blocking=True)
+                in_done.append(torch.cuda.Event())
+                in_done[-1].record(s_in)
+                s_cmp.wait_event(in_done[i])
+                if i >= 2:
+                    s_cmp.wait_event(out_done[i - 2])  # step i-2's outputs in this set are on the host
+                kernels(ins, outs, s_cmp.cuda_stream)
+                cmp_done.append(torch.cuda.Event())
+                cmp_done[-1].record(s_cmp)
+                s_out.wait_event(cmp_done[i])
+                with torch.cuda.stream(s_out):
+                    for hd, dd in zip(outs_h, outs):
+                        hd.copy_(dd, non_blocking=True)
+                out_done.append(torch.cuda.Event())
+                out_done[-1].record(s_out)
+            if e_end is not None:
+                for e in out_done + cmp_done:
+                    s_out.wait_event(e)
+                e_end.record(s_out)
 
         n_e2e = max(3, args.steps // 2)
-        for _ in range(2):
-            e2e_step()
+        torch.cuda.synchronize()
+        pipeline(3)
         torch.cuda.synchronize()
         e0, e1 = ev(), ev()
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        pipeline(n_e2e, e0, e1)
         torch.cuda.synchronize()
+        if fa.fa_last_device_status(sptr) != fa.FA_OK:
+            raise RuntimeError("device status reports a timed-out wait (end-to-end leg)")
         ms = e0.elapsed_time(e1)
         out["e2e"] = {"value": (fwd_f + bwd_f) * n_e2e / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
-                      "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h), "ms_per_step": ms / n_e2e}
+                      "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h), "ms_per_step": ms / n_e2e,
+                      "schedule": "three streams: uploads of step i, kernels of step i-1, downloads of step i-2 "
+                                  "overlap; two device buffer sets"}
+        if not torch.equal(outs_h[0], first_out[0].cpu()) and not torch.equal(outs_h[0], sets[1][1][0].cpu()):
+            raise RuntimeError("end-to-end output differs from the device result")
     if not args.no_cpu_baseline:
         import oracle
 
