@@ -51,7 +51,7 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale) {
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
-  // element offsets of [B, N, H, d] must fit the 2^31 range used for row indices
+  // fewer than 2^40 elements: offsets are 64-bit, and this keeps them far from overflow
   if ((long long)B * N * H * d >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
