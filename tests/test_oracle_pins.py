@@ -308,3 +308,31 @@ def test_oracle_results_do_not_depend_on_its_thread_count(oracle_mod):
         oracle_mod.set_threads(n)
     for a, b in zip(full + tuple(grads), one + tuple(grads1)):
         assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- automatic differentiation
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", [(2, 37, 4, 2, 16, False), (2, 37, 4, 2, 16, True),
+                                                (1, 64, 2, 1, 32, True), (1, 1, 1, 1, 8, True)])
+def test_backward_matches_autograd_of_the_definition(oracle_mod, B, N, H, Hkv, d, causal):
+    """The oracle's backward (row terms D = rowsum(dO o O), dS = P o (dP - D)) against
+    torch's automatic differentiation of softmax(scale Q K^T + mask) V in float64, and its
+    LSE against torch.logsumexp: two computations that share nothing with the oracle."""
+    torch = pytest.importorskip("torch")
+    q, k, v = qkv(B, N, H, Hkv, d, 150 + N + causal)
+    dO = rnd(q.shape, 151)
+    s = 1.0 / math.sqrt(d)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    g = H // Hkv
+    kk = tk.repeat_interleave(g, dim=2)  # query head h reads kv head h // g
+    vv = tv.repeat_interleave(g, dim=2)
+    scores = torch.einsum("bihc,bjhc->bhij", tq, kk) * s
+    if causal:
+        scores = scores.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    o = torch.einsum("bhij,bjhc->bihc", torch.softmax(scores, dim=-1), vv)
+    (o * torch.tensor(dO)).sum().backward()
+    o1, l1 = oracle_mod.attention_fwd(q, k, v, s, causal)
+    np.testing.assert_allclose(o1, o.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, torch.logsumexp(scores, dim=-1).detach().numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = oracle_mod.attention_bwd(q, k, v, dO, s, causal)
+    for name, a, t in (("dq", dq, tq), ("dk", dk, tk), ("dv", dv, tv)):
+        np.testing.assert_allclose(a, t.grad.numpy(), rtol=0, atol=1e-11, err_msg=name)
